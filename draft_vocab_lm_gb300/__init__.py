@@ -1,1 +1,256 @@
-"""GB300-native draft-head argmax library (Python binding; filled in below)."""
+"""GB300-native draft-head argmax: Python binding of libdvl.so.
+
+The library computes, for M hidden rows of a speculative-decoding draft head,
+the best token of logits = h . W^T over a bf16 or NVFP4 head -- the full
+vocabulary or a frequency-ranked shortlist with its d2t map -- fused on the
+device so no logit tensor is written (see include/dvl.h for the C ABI).
+
+This module only marshals arguments: PyTorch provides device memory and the
+current CUDA stream, and every step of the computation runs in the library's
+CUDA kernels.  There is no CPU fallback; calls fail loudly if the library is
+not built.
+
+    head = Head(w, V=248_320, d2t=d2t)            # w: CUDA bf16 [N][K]
+    ids, logits = draft_argmax(head, h)            # h: CUDA bf16 [M][K]
+    ids, logits = draft_topk(head, h, k=4)
+    w_trim, _, d2t, n_dup = trim_head(w_full, ranks)
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import roofline
+from ._native import (DVL_BF16, DVL_K_MULTIPLE, DVL_MAX_K, DVL_MAX_M, DVL_MAX_TOPK,
+                      DVL_NVFP4, DvlError, DvlHead, check, lib)
+
+__all__ = [
+    "Head", "DvlError", "draft_argmax", "draft_topk", "trim_head", "workspace_bytes",
+    "make_workspace", "workspace_init", "histogram", "build_ranks", "union_sorted",
+    "read_ranks_txt", "write_ranks_txt", "roofline", "version",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream, device) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def version() -> int:
+    return int(lib().dvl_version())
+
+
+class Head:
+    """A draft head resident on one CUDA device.
+
+    w:        bf16 [N][K] (any 2-byte dtype holding bfloat16 bits), or for
+              NVFP4 uint8 codes [N][K/2] (two E2M1 per byte, low nibble = even k).
+    V:        full vocabulary size (ids lie in [0, V)); defaults to N.
+    d2t:      int32 [N] full-vocabulary id of each row, or None (identity,
+              shifted by id_base).
+    scales:   NVFP4 only: uint8 E4M3 [N][K/16].
+    global_scale: NVFP4 tensor scale.
+    """
+
+    def __init__(self, w, *, V: int | None = None, d2t=None, scales=None,
+                 global_scale: float = 1.0, id_base: int = 0):
+        torch = _torch()
+        if not w.is_cuda or w.dim() != 2 or not w.is_contiguous():
+            raise ValueError("w must be a contiguous 2-D CUDA tensor")
+        if scales is not None:
+            if w.element_size() != 1:
+                raise ValueError("NVFP4 codes must be a uint8 tensor")
+            self.dtype = DVL_NVFP4
+            self.K = 2 * w.shape[1]
+            if (not scales.is_cuda or not scales.is_contiguous()
+                    or tuple(scales.shape) != (w.shape[0], self.K // 16)):
+                raise ValueError("scales must be a contiguous CUDA uint8 [N][K/16] tensor")
+        else:
+            if w.element_size() != 2:
+                raise ValueError("a bf16 head needs a 2-byte dtype")
+            self.dtype = DVL_BF16
+            self.K = w.shape[1]
+        self.w = w
+        self.scales = scales
+        self.N = w.shape[0]
+        self.V = int(V) if V is not None else self.N
+        self.id_base = int(id_base)
+        self.global_scale = float(global_scale)
+        if d2t is not None:
+            if (not d2t.is_cuda or d2t.dtype != torch.int32 or not d2t.is_contiguous()
+                    or tuple(d2t.shape) != (self.N,)):
+                raise ValueError("d2t must be a contiguous CUDA int32 [N] tensor")
+        self.d2t = d2t
+        self.device = w.device
+
+    def struct(self) -> DvlHead:
+        s = DvlHead()
+        s.dtype = self.dtype
+        s.N = self.N
+        s.K = self.K
+        s.V = self.V
+        s.id_base = self.id_base
+        s.w = self.w.data_ptr()
+        s.scales = self.scales.data_ptr() if self.scales is not None else None
+        s.global_scale = self.global_scale
+        s.d2t = self.d2t.data_ptr() if self.d2t is not None else None
+        return s
+
+    def slice_rows(self, n0: int, n1: int) -> "Head":
+        """Rows [n0, n1) as a head of their own (views, no copy); ids keep
+        their full-vocabulary values."""
+        h = Head.__new__(Head)
+        h.__dict__.update(self.__dict__)
+        h.w = self.w[n0:n1]
+        h.scales = self.scales[n0:n1] if self.scales is not None else None
+        h.d2t = self.d2t[n0:n1] if self.d2t is not None else None
+        h.id_base = self.id_base + (n0 if self.d2t is None else 0)
+        h.N = n1 - n0
+        return h
+
+
+def workspace_bytes(M: int, k: int = 1) -> int:
+    return int(lib().dvl_workspace_bytes(int(M), int(k)))
+
+
+def workspace_init(ws, stream=None) -> None:
+    check("dvl_workspace_init",
+          lib().dvl_workspace_init(ws.data_ptr(), ws.numel() * ws.element_size(),
+                                   _stream_handle(stream, ws.device)))
+
+
+def make_workspace(M: int = DVL_MAX_M, k: int = DVL_MAX_TOPK, device=None, stream=None):
+    """A zeroed device workspace big enough for calls with up to M rows and k."""
+    torch = _torch()
+    n = workspace_bytes(M, k)
+    if n == 0:
+        raise ValueError("M or k outside the library's limits")
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    workspace_init(ws, stream)
+    return ws
+
+
+def _check_h(head: Head, h):
+    if not h.is_cuda or h.dim() != 2 or not h.is_contiguous() or h.element_size() != 2:
+        raise ValueError("h must be a contiguous 2-D CUDA bf16 tensor")
+    if h.shape[1] != head.K:
+        raise ValueError("h width must equal the head's K")
+
+
+def draft_topk(head: Head, h, k: int, *, ids=None, logits=None, ws=None, stream=None):
+    """Per hidden row: the k best (full id, logit), best first."""
+    torch = _torch()
+    _check_h(head, h)
+    M = h.shape[0]
+    if ids is None:
+        ids = torch.empty((M, k), dtype=torch.int32, device=h.device)
+    if logits is None:
+        logits = torch.empty((M, k), dtype=torch.float32, device=h.device)
+    if ws is None:
+        ws = make_workspace(M, k, device=h.device, stream=stream)
+    st = head.struct()
+    check("dvl_draft_topk",
+          lib().dvl_draft_topk(ctypes.byref(st), h.data_ptr(), M, int(k), ids.data_ptr(),
+                               logits.data_ptr(), ws.data_ptr(), ws.numel(),
+                               _stream_handle(stream, h.device)))
+    return ids, logits
+
+
+def draft_argmax(head: Head, h, *, ids=None, logits=None, ws=None, stream=None):
+    """Per hidden row: (full id, max logit) of the best head row."""
+    torch = _torch()
+    _check_h(head, h)
+    M = h.shape[0]
+    if ids is None:
+        ids = torch.empty(M, dtype=torch.int32, device=h.device)
+    if logits is None:
+        logits = torch.empty(M, dtype=torch.float32, device=h.device)
+    if ws is None:
+        ws = make_workspace(M, 1, device=h.device, stream=stream)
+    st = head.struct()
+    check("dvl_draft_argmax",
+          lib().dvl_draft_argmax(ctypes.byref(st), h.data_ptr(), M, ids.data_ptr(),
+                                 logits.data_ptr(), ws.data_ptr(), ws.numel(),
+                                 _stream_handle(stream, h.device)))
+    return ids, logits
+
+
+def trim_head(w_full, ranks, *, scales=None, stream=None):
+    """Gather the rows `ranks` names (in its order) from a full head.
+
+    w_full: CUDA bf16 [V][K] or NVFP4 codes [V][K/2] (then `scales` [V][K/16]).
+    ranks:  host ids (list, NumPy or CPU tensor).
+    Returns (w_trim, scales_trim or None, d2t int32 CUDA [n], n_duplicates)."""
+    torch = _torch()
+    r = np.ascontiguousarray(np.asarray(ranks, dtype=np.int32))
+    n = r.shape[0]
+    full = Head(w_full, scales=scales)
+    w_trim = torch.empty((n, w_full.shape[1]), dtype=w_full.dtype, device=w_full.device)
+    s_trim = None
+    if scales is not None:
+        s_trim = torch.empty((n, scales.shape[1]), dtype=scales.dtype, device=scales.device)
+    d2t = torch.empty(n, dtype=torch.int32, device=w_full.device)
+    dup = ctypes.c_int32(0)
+    st = full.struct()
+    check("dvl_trim_head",
+          lib().dvl_trim_head(ctypes.byref(st), r.ctypes.data, n, w_trim.data_ptr(),
+                              s_trim.data_ptr() if s_trim is not None else None,
+                              d2t.data_ptr(), ctypes.byref(dup),
+                              _stream_handle(stream, w_full.device)))
+    return w_trim, s_trim, d2t, int(dup.value)
+
+
+# ---------------------------------------------------------------------------
+# Host-only ranks builder
+# ---------------------------------------------------------------------------
+
+def histogram(tokens, V: int, counts: np.ndarray | None = None) -> np.ndarray:
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    if counts is None:
+        counts = np.zeros(V, dtype=np.int64)
+    assert counts.dtype == np.int64 and counts.flags["C_CONTIGUOUS"] and counts.shape == (V,)
+    check("dvl_histogram", lib().dvl_histogram(t.ctypes.data, t.shape[0], V, counts.ctypes.data))
+    return counts
+
+
+def build_ranks(counts: np.ndarray, N: int, forced=None, sorted_ids: bool = False) -> np.ndarray:
+    c = np.ascontiguousarray(counts, dtype=np.int64)
+    f = np.ascontiguousarray(np.asarray([] if forced is None else forced, dtype=np.int32))
+    out = np.empty(max(1, min(N, c.shape[0])), dtype=np.int32)
+    n = ctypes.c_int32(0)
+    check("dvl_build_ranks",
+          lib().dvl_build_ranks(c.ctypes.data, c.shape[0], f.ctypes.data if f.size else None,
+                                f.shape[0], int(N), 1 if sorted_ids else 0, out.ctypes.data,
+                                ctypes.byref(n)))
+    return out[:n.value].copy()
+
+
+def union_sorted(a, b) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    b = np.ascontiguousarray(np.asarray(b, dtype=np.int32))
+    out = np.empty(max(1, a.shape[0] + b.shape[0]), dtype=np.int32)
+    n = ctypes.c_int32(0)
+    check("dvl_union_sorted",
+          lib().dvl_union_sorted(a.ctypes.data if a.size else None, a.shape[0],
+                                 b.ctypes.data if b.size else None, b.shape[0],
+                                 out.ctypes.data, ctypes.byref(n)))
+    return out[:n.value].copy()
+
+
+def read_ranks_txt(path: str) -> np.ndarray:
+    """A ranks list: one decimal id per line (blank lines ignored)."""
+    with open(path) as f:
+        return np.array([int(x) for x in f if x.strip()], dtype=np.int32)
+
+
+def write_ranks_txt(path: str, ids) -> None:
+    with open(path, "w") as f:
+        f.writelines(f"{int(x)}\n" for x in ids)

@@ -1,0 +1,253 @@
+// The C ABI: argument checks, workspace handling, dispatch to the kernels.
+// Every check runs on the host before anything is enqueued; nothing here
+// allocates, frees or synchronizes.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "dvl.h"
+#include "dvl_internal.h"
+
+namespace dvl {
+
+namespace {
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_dev;
+std::map<std::tuple<const void *, int, size_t>, int> g_occ;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+}  // namespace
+
+cudaError_t device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    {
+        std::lock_guard<std::mutex> g(g_mu);
+        auto it = g_dev.find(dev);
+        if (it != g_dev.end()) {
+            *out = it->second;
+            return cudaSuccess;
+        }
+    }
+    DeviceInfo di;
+    e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    e = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> g(g_mu);
+    g_dev[dev] = di;
+    *out = di;
+    return cudaSuccess;
+}
+
+cudaError_t blocks_per_sm(const void *func, int threads, size_t smem, int *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const auto key = std::make_tuple(func, dev, smem);
+    {
+        std::lock_guard<std::mutex> g(g_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) {
+            *out = it->second;
+            return cudaSuccess;
+        }
+    }
+    DeviceInfo di;
+    e = device_info(&di);
+    if (e != cudaSuccess)
+        return e;
+    if (smem > (size_t)di.smem_optin)
+        return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> g(g_mu);
+    g_occ[key] = n;
+    *out = n;
+    return cudaSuccess;
+}
+
+namespace {
+
+dvl_status check_head(const dvl_head *hd)
+{
+    if (!hd)
+        return DVL_ERR_INVALID_ARG;
+    if (hd->dtype != DVL_BF16 && hd->dtype != DVL_NVFP4)
+        return DVL_ERR_INVALID_ARG;
+    if (hd->reserved != 0 || hd->reserved2 != 0)
+        return DVL_ERR_INVALID_ARG;
+    if (hd->N < 1 || hd->K < DVL_K_MULTIPLE || hd->K % DVL_K_MULTIPLE != 0 || hd->K > DVL_MAX_K)
+        return DVL_ERR_INVALID_ARG;
+    if (hd->V < 1 || hd->V > 0x7fffffffLL)
+        return DVL_ERR_INVALID_ARG;
+    if (!hd->w || !aligned(hd->w, 16))
+        return DVL_ERR_INVALID_ARG;
+    if (hd->dtype == DVL_NVFP4 && (!hd->scales || !aligned(hd->scales, 16)))
+        return DVL_ERR_INVALID_ARG;
+    if (hd->d2t) {
+        if (!aligned(hd->d2t, 4))
+            return DVL_ERR_INVALID_ARG;
+    } else if (hd->id_base < 0 || hd->id_base + hd->N > hd->V) {
+        return DVL_ERR_INVALID_ARG;
+    }
+    return DVL_OK;
+}
+
+dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, int32_t *ids,
+                       float *logits, void *ws, size_t ws_bytes, void *stream)
+{
+    dvl_status st = check_head(hd);
+    if (st != DVL_OK)
+        return st;
+    if (M < 1 || M > DVL_MAX_M || k < 1 || k > DVL_MAX_TOPK || k > hd->N)
+        return DVL_ERR_INVALID_ARG;
+    if (!h || !aligned(h, 16) || !ids || !aligned(ids, 4) || !logits || !aligned(logits, 4))
+        return DVL_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, 16) || ws_bytes < dvl_workspace_bytes(M, k))
+        return DVL_ERR_WORKSPACE;
+    const int chunk =
+        hd->dtype == DVL_BF16 ? max_chunk_rows_bf16(hd->K) : max_chunk_rows_nvfp4(hd->K);
+    if (chunk < 1)
+        return DVL_ERR_UNSUPPORTED;
+    ArgmaxArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.w = hd->w;
+    a.scales = hd->scales;
+    a.gscale = hd->global_scale;
+    a.d2t = hd->d2t;
+    a.id_base = hd->id_base;
+    a.N = hd->N;
+    a.K = hd->K;
+    a.k = k;
+    a.ws = static_cast<unsigned char *>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int kmax = k == 1 ? 1 : DVL_MAX_TOPK;
+    for (int m0 = 0; m0 < M; m0 += chunk) {
+        const int mc = M - m0 < chunk ? M - m0 : chunk;
+        a.h = static_cast<const uint16_t *>(h) + (size_t)m0 * hd->K;
+        a.ids = ids + (size_t)m0 * k;
+        a.logits = logits + (size_t)m0 * k;
+        cudaError_t e = hd->dtype == DVL_BF16 ? launch_argmax_bf16(a, mc, kmax, s)
+                                              : launch_argmax_nvfp4(a, mc, kmax, s);
+        if (e != cudaSuccess)
+            return DVL_ERR_CUDA;
+    }
+    return DVL_OK;
+}
+
+}  // namespace
+}  // namespace dvl
+
+using namespace dvl;
+
+extern "C" {
+
+const char *dvl_status_string(int status)
+{
+    switch (status) {
+    case DVL_OK: return "ok";
+    case DVL_ERR_INVALID_ARG: return "invalid argument";
+    case DVL_ERR_OUT_OF_RANGE: return "id out of range";
+    case DVL_ERR_UNSUPPORTED: return "unsupported shape";
+    case DVL_ERR_WORKSPACE: return "workspace missing or too small";
+    case DVL_ERR_CUDA: return "CUDA error";
+    case DVL_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int dvl_version(void) { return 100; }
+
+size_t dvl_workspace_bytes(int32_t M, int32_t k)
+{
+    if (M < 1 || M > DVL_MAX_M || k < 1 || k > DVL_MAX_TOPK)
+        return 0;
+    size_t b = kWsSlots;
+    if (k > 1)
+        b += (size_t)kMaxCtas * (size_t)M * DVL_MAX_TOPK * sizeof(uint64_t);
+    return b;
+}
+
+dvl_status dvl_workspace_init(void *ws, size_t bytes, void *stream)
+{
+    if (!ws || !aligned(ws, 16) || bytes < kWsSlots)
+        return DVL_ERR_WORKSPACE;
+    if (cudaMemsetAsync(ws, 0, bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DVL_ERR_CUDA;
+    return DVL_OK;
+}
+
+dvl_status dvl_draft_argmax(const dvl_head *head, const void *h, int32_t M, int32_t *ids,
+                            float *max_logit, void *ws, size_t ws_bytes, void *stream)
+{
+    return reduce_call(head, h, M, 1, ids, max_logit, ws, ws_bytes, stream);
+}
+
+dvl_status dvl_draft_topk(const dvl_head *head, const void *h, int32_t M, int32_t k,
+                          int32_t *ids, float *logits, void *ws, size_t ws_bytes, void *stream)
+{
+    return reduce_call(head, h, M, k, ids, logits, ws, ws_bytes, stream);
+}
+
+dvl_status dvl_trim_head(const dvl_head *full, const int32_t *ranks, int32_t n_ranks,
+                         void *w_trim, uint8_t *scales_trim, int32_t *d2t,
+                         int32_t *n_duplicates, void *stream)
+{
+    dvl_status st = check_head(full);
+    if (st != DVL_OK)
+        return st;
+    if ((int64_t)full->N != full->V || full->d2t || full->id_base != 0)
+        return DVL_ERR_INVALID_ARG;
+    if (!ranks || n_ranks < 1 || !w_trim || !aligned(w_trim, 16) || !d2t || !aligned(d2t, 4))
+        return DVL_ERR_INVALID_ARG;
+    if (full->dtype == DVL_NVFP4 && (!scales_trim || !aligned(scales_trim, 16)))
+        return DVL_ERR_INVALID_ARG;
+    std::vector<unsigned char> seen((size_t)full->V, 0);
+    int32_t dup = 0;
+    for (int32_t i = 0; i < n_ranks; ++i) {
+        const int32_t r = ranks[i];
+        if (r < 0 || (int64_t)r >= full->V)
+            return DVL_ERR_OUT_OF_RANGE;
+        if (seen[(size_t)r])
+            ++dup;
+        seen[(size_t)r] = 1;
+    }
+    if (n_duplicates)
+        *n_duplicates = dup;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(d2t, ranks, (size_t)n_ranks * sizeof(int32_t), cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+        return DVL_ERR_CUDA;
+    const int64_t K = full->K;
+    cudaError_t e;
+    if (full->dtype == DVL_BF16) {
+        e = launch_trim_rows(static_cast<const unsigned char *>(full->w), K * 2,
+                             static_cast<unsigned char *>(w_trim), d2t, n_ranks, s);
+    } else {
+        e = launch_trim_rows(static_cast<const unsigned char *>(full->w), K / 2,
+                             static_cast<unsigned char *>(w_trim), d2t, n_ranks, s);
+        if (e == cudaSuccess)
+            e = launch_trim_rows(full->scales, K / 16, scales_trim, d2t, n_ranks, s);
+    }
+    return e == cudaSuccess ? DVL_OK : DVL_ERR_CUDA;
+}
+
+}  // extern "C"

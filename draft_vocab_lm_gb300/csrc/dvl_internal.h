@@ -1,0 +1,58 @@
+// Internal host-side declarations shared by the C ABI and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace dvl {
+
+// Workspace layout (device bytes).  Every kernel call leaves it as it found
+// it: the ticket wraps back to 0 and the best keys are exchanged back to 0.
+constexpr int kMaxCtas = 1024;            // grid cap of every reducing kernel
+constexpr size_t kWsTicket = 0;           // uint32: blocks finished so far
+constexpr size_t kWsStatus = 4;           // uint32: reserved for device checks
+constexpr size_t kWsBest = 256;           // uint64[DVL_MAX_M]: best key per row (k = 1)
+constexpr size_t kWsSlots = 512;          // uint64[kMaxCtas][M][kmax] (k > 1)
+
+// Arguments of one reducing launch (one chunk of at most 8 hidden rows).
+struct ArgmaxArgs {
+    const void *w;            // bf16 [N][K] or NVFP4 codes [N][K/2]
+    const uint8_t *scales;    // NVFP4 E4M3 [N][K/16]
+    float gscale;             // NVFP4 tensor scale
+    const int32_t *d2t;       // int32 [N] or nullptr
+    int64_t id_base;          // full id of row 0 when d2t is null
+    int N, K, Kpad;           // Kpad: K rounded up to the kernel's k-step
+    const uint16_t *h;        // bf16 [M][K] of this chunk
+    int32_t *ids;             // [M][k] of this chunk
+    float *logits;            // [M][k] of this chunk
+    int k;                    // results per row (1 .. kmax)
+    unsigned char *ws;        // workspace base
+};
+
+// Per-device facts, queried once.
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+cudaError_t device_info(DeviceInfo *out);
+
+// Blocks of `func` (launched with `threads` threads and `smem` dynamic shared
+// bytes) resident per SM on the current device.  The first query per (kernel,
+// device, smem) also raises the kernel's dynamic shared-memory limit; the
+// answer is cached.
+cudaError_t blocks_per_sm(const void *func, int threads, size_t smem, int *out);
+
+// Launchers (return the launch's cudaError_t).  M is the chunk's row count
+// (1 .. 8), kmax is 1 (argmax) or 4 (top-k).
+cudaError_t launch_argmax_bf16(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
+cudaError_t launch_argmax_nvfp4(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
+int max_chunk_rows_bf16(int K);
+int max_chunk_rows_nvfp4(int K);
+
+cudaError_t launch_trim_rows(const unsigned char *src, int64_t src_row_bytes,
+                             unsigned char *dst, const int32_t *ranks, int n,
+                             cudaStream_t s);
+
+}  // namespace dvl

@@ -1,0 +1,203 @@
+/*
+ * dvl.h -- C ABI of the GB300 draft-head argmax library (libdvl.so).
+ *
+ * The operation: a speculative-decoding draft head projects M hidden rows
+ * h[M][K] against the rows of its LM head W[N][K] and keeps, per hidden row,
+ * the best token -- logits = h . W^T, reduced on the device to an id and its
+ * logit, so no logit tensor is ever written to memory.  N is either the full
+ * vocabulary or a frequency-ranked shortlist of it, in which case a d2t map
+ * turns a shortlist row index into a full-vocabulary id.
+ *   - the projection and its shape ("Shortlist MTP", section "What I was
+ *     testing": hidden width 2,560 against 248,320 rows; M is 1 for a draft
+ *     step and 3 for an MTP2 verify step);
+ *   - the shortlist and its on-device reduction ("Shortlist MTP", sections
+ *     "What was actually happening" and "Re-running the comparison fairly":
+ *     the shortlist projection and local argmax reduction);
+ *   - the trim at load and the d2t map ("Masked MTP drafts": a ranks .txt
+ *     next to the model, the head weight trimmed at load; EAGLE-3's d2t
+ *     index mapping reused for a frequency-ranked subset);
+ *   - the NVFP4 head ("Masked MTP drafts": the trimmed head requantized to
+ *     NVFP4);
+ *   - the ranks builder ("Shortlist MTP", section "Building the 16k
+ *     shortlist"; "[DGX Spark] Qwen3.8-Flash-Next on two DGX Sparks",
+ *     section "Build the draft vocabulary from your own text").
+ *
+ * Conventions for every entry point:
+ *   - Memory: the caller owns every buffer.  "device" pointers are CUDA
+ *     device memory on the current device; "host" pointers are ordinary host
+ *     memory.  The GPU entry points never allocate, free or synchronize; they
+ *     enqueue work on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and return.  Results are ready in stream order.
+ *   - Errors: arguments are checked on the host before anything is enqueued;
+ *     a bad argument returns a non-zero dvl_status and enqueues nothing.  A
+ *     failed launch returns DVL_ERR_CUDA (the outputs are then undefined).
+ *   - Threading: calls are thread-safe.  One workspace serves one stream at a
+ *     time: two calls that may run concurrently on the GPU must not share a
+ *     workspace.
+ *   - Alignment: W, h, scales and the workspace start on 16-byte boundaries;
+ *     d2t, ids and logits on 4-byte boundaries.
+ */
+#ifndef DVL_H
+#define DVL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DVL_OK = 0,
+    DVL_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, misalignment        */
+    DVL_ERR_OUT_OF_RANGE = 2, /* an id outside [0, V)                        */
+    DVL_ERR_UNSUPPORTED = 3,  /* a shape this build has no kernel for        */
+    DVL_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required  */
+    DVL_ERR_CUDA = 5,         /* a CUDA runtime call or a launch failed      */
+    DVL_ERR_TIMEOUT = 6       /* reserved: a bounded device wait gave up     */
+} dvl_status;
+
+typedef enum {
+    DVL_BF16 = 0,  /* W: bfloat16 [N][K] row-major                          */
+    DVL_NVFP4 = 1  /* W: E2M1 codes [N][K/2] (low nibble = even k), E4M3
+                      scales [N][K/16] (one per 16 consecutive k of a row),
+                      one fp32 tensor scale                                  */
+} dvl_dtype;
+
+/* Limits of this build. */
+#define DVL_MAX_M 32        /* hidden rows per call                            */
+#define DVL_MAX_TOPK 4      /* k of draft_topk                                 */
+#define DVL_K_MULTIPLE 64   /* K must be a positive multiple of this           */
+#define DVL_MAX_K 24576     /* largest hidden width                            */
+
+/* A draft head as the kernels read it.  Every pointer is device memory. */
+typedef struct dvl_head {
+    int32_t dtype;        /* dvl_dtype                                         */
+    int32_t N;            /* rows of W (>= 1)                                  */
+    int32_t K;            /* hidden width (multiple of 64, <= DVL_MAX_K)       */
+    int32_t reserved;     /* must be 0                                         */
+    int64_t V;            /* full vocabulary size: ids lie in [0, V)           */
+    int64_t id_base;      /* with d2t == NULL, row n has full id id_base + n;
+                             id_base + N <= V.  0 for a whole head; the first
+                             id of a slice when a head is split by rows.       */
+    const void *w;        /* bf16 [N][K], or NVFP4 codes [N][K/2]              */
+    const uint8_t *scales;/* NVFP4: E4M3 [N][K/16]; NULL for bf16              */
+    float global_scale;   /* NVFP4 tensor scale; ignored for bf16              */
+    int32_t reserved2;    /* must be 0                                         */
+    const int32_t *d2t;   /* int32 [N]: full-vocabulary id of each row, each in
+                             [0, V) (the kernels do not check); NULL means the
+                             identity map shifted by id_base                   */
+} dvl_head;
+
+/* Human-readable name of a status code (static storage). */
+const char *dvl_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dvl_version(void);
+
+/* ---------------------------------------------------------------------- */
+/* Workspace                                                              */
+/* ---------------------------------------------------------------------- */
+
+/* Bytes of device workspace one draft_argmax (k = 1) or draft_topk call
+ * with M hidden rows needs.  Returns 0 for M or k outside their limits.
+ * The workspace holds the cross-block reduction state: a ticket counter,
+ * the per-row best keys and, for k > 1, one candidate list per thread block.
+ * It is self-cleaning: every call leaves it as it found it. */
+size_t dvl_workspace_bytes(int32_t M, int32_t k);
+
+/* Zero a workspace before its first use (enqueued on `stream`).  Only
+ * needed once; also restores a workspace whose last call did not complete.
+ * ws: device, 16-byte aligned; bytes >= dvl_workspace_bytes(M, k) of every
+ * call that will use it. */
+dvl_status dvl_workspace_init(void *ws, size_t bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* The hot path                                                           */
+/* ---------------------------------------------------------------------- */
+
+/* Per hidden row m: the full-vocabulary id of the head row with the largest
+ * logit sum_k W[n][k] * h[m][k], and that logit.  The dot products run in
+ * fp32 on the device (products of bf16 values are exact; the order of the
+ * additions is the kernel's).  Exactly equal logits go to the lowest full
+ * id; a NaN logit never wins (a row whose every logit is NaN yields id -1
+ * and a NaN logit); -0 and +0 compare equal and +0 is reported.  For NVFP4,
+ * weight = e2m1(code) * e4m3(scale) * global_scale, and the kernel applies
+ * global_scale to the finished dot product.
+ *   head:      the head (see dvl_head); host struct, device pointers.
+ *   h:         device bf16 [M][K], row-major.
+ *   M:         1 .. DVL_MAX_M.
+ *   ids:       device int32 [M] (out).
+ *   max_logit: device fp32 [M] (out).
+ *   ws:        device workspace of at least dvl_workspace_bytes(M, 1)
+ *              bytes, zeroed once by dvl_workspace_init.
+ * Errors: DVL_ERR_INVALID_ARG (NULL, misaligned, N < 1, K not a multiple of
+ * 64 or above DVL_MAX_K, M out of range, reserved fields non-zero, dtype
+ * unknown, NVFP4 without scales, d2t == NULL with id_base + N > V),
+ * DVL_ERR_WORKSPACE, DVL_ERR_CUDA. */
+dvl_status dvl_draft_argmax(const dvl_head *head, const void *h, int32_t M,
+                            int32_t *ids, float *max_logit, void *ws,
+                            size_t ws_bytes, void *stream);
+
+/* Per hidden row m: the k best head rows by (logit desc, full id asc), as
+ * full ids and logits, best first.  Same arithmetic, rules and errors as
+ * dvl_draft_argmax; k = 1 gives exactly its result.  Rows are distinct; a
+ * d2t that repeats an id can make an id appear twice.
+ *   k:      1 .. DVL_MAX_TOPK, and k <= N.
+ *   ids:    device int32 [M][k] (out).
+ *   logits: device fp32 [M][k] (out).
+ *   ws:     at least dvl_workspace_bytes(M, k) bytes. */
+dvl_status dvl_draft_topk(const dvl_head *head, const void *h, int32_t M, int32_t k,
+                          int32_t *ids, float *logits, void *ws, size_t ws_bytes,
+                          void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Load time                                                              */
+/* ---------------------------------------------------------------------- */
+
+/* Trim a full head to the rows a ranks list names, in the list's order:
+ * W_trim[i] = W_full[ranks[i]] (byte copy of the row; for NVFP4 the codes
+ * and the scales), d2t[i] = ranks[i].  The ranks are checked on the host
+ * before anything is enqueued; duplicates are accepted (padded lists exist)
+ * and counted.
+ *   full:      the full head: N == V, d2t == NULL, id_base == 0.
+ *   ranks:     HOST int32 [n_ranks], each in [0, V).
+ *   n_ranks:   >= 1.
+ *   w_trim:    device, rows of the same format: bf16 [n][K] or codes [n][K/2].
+ *   scales_trim: device E4M3 [n][K/16] for NVFP4; NULL for bf16.
+ *   d2t:       device int32 [n_ranks] (out); the trimmed head's d2t.
+ *   n_duplicates: HOST (out, may be NULL): entries that repeat an earlier id.
+ * The ranks are copied to d2t with a host-to-device copy from pageable
+ * memory, which returns once the source has been read.
+ * Errors: DVL_ERR_INVALID_ARG, DVL_ERR_OUT_OF_RANGE (nothing enqueued),
+ * DVL_ERR_CUDA. */
+dvl_status dvl_trim_head(const dvl_head *full, const int32_t *ranks, int32_t n_ranks,
+                         void *w_trim, uint8_t *scales_trim, int32_t *d2t,
+                         int32_t *n_duplicates, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Host-only ranks builder (no GPU involved)                              */
+/* ---------------------------------------------------------------------- */
+
+/* counts[t] += 1 for every token t of tokens[0..n).  All host memory.
+ * DVL_ERR_OUT_OF_RANGE (nothing counted) if a token lies outside [0, V). */
+dvl_status dvl_histogram(const int32_t *tokens, int64_t n, int64_t V, int64_t *counts);
+
+/* A shortlist of N ids from a histogram: the distinct forced ids first, in
+ * rank order, then the other ids in rank order, cut at N (rank order =
+ * higher count first, then lower id).  sorted != 0 sorts the result by id.
+ * All host memory; ranks_out holds min(N, V) entries; *n_out receives that
+ * count.  DVL_ERR_OUT_OF_RANGE if a forced id lies outside [0, V). */
+dvl_status dvl_build_ranks(const int64_t *counts, int64_t V, const int32_t *forced,
+                           int32_t n_forced, int32_t N, int32_t sorted,
+                           int32_t *ranks_out, int32_t *n_out);
+
+/* The sorted set union of two id lists (each taken as a set).  All host
+ * memory; out holds na + nb entries; *n_out receives the union's size. */
+dvl_status dvl_union_sorted(const int32_t *a, int32_t na, const int32_t *b, int32_t nb,
+                            int32_t *out, int32_t *n_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DVL_H */

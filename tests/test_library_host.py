@@ -1,0 +1,150 @@
+"""CPU-side checks of the C-ABI library: it loads, exports every symbol the
+header declares, its host-only ranks builder matches the oracle's, and the
+argument checks reject bad calls before touching the GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+import synthetic as S
+
+
+@pytest.fixture(scope="session")
+def dvl():
+    from draft_vocab_lm_gb300 import build
+    build.build()
+    import draft_vocab_lm_gb300 as d
+    return d
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "dvl.h")).read()
+    return sorted(set(re.findall(r"\b(dvl_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(dvl):
+    from draft_vocab_lm_gb300 import _native
+    lib = _native.lib()
+    declared = _declared_symbols()
+    assert set(declared) == set(_native.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert dvl.version() == 100
+    assert lib.dvl_status_string(0) == b"ok"
+    assert lib.dvl_status_string(4) == b"workspace missing or too small"
+
+
+def test_workspace_bytes(dvl):
+    assert dvl.workspace_bytes(1, 1) == 512
+    assert dvl.workspace_bytes(32, 1) == 512
+    assert dvl.workspace_bytes(3, 4) == 512 + 1024 * 3 * 4 * 8
+    assert dvl.workspace_bytes(0, 1) == 0
+    assert dvl.workspace_bytes(33, 1) == 0
+    assert dvl.workspace_bytes(1, 5) == 0
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_build_ranks_matches_oracle(dvl, oracle_mod, seed):
+    rng = np.random.default_rng(seed)
+    V = 5000
+    tokens = S.zipf_tokens(seed, V, 40_000)
+    c_lib = dvl.histogram(tokens, V)
+    c_or = oracle_mod.histogram(tokens, V)
+    assert np.array_equal(c_lib, c_or)
+    forced = rng.integers(0, V, size=300).astype(np.int32)
+    for N in (1, 100, 2500, V, V + 10):
+        for srt in (False, True):
+            a = dvl.build_ranks(c_lib, N, forced, sorted_ids=srt)
+            b = oracle_mod.build_ranks(c_or, N, forced, sorted_ids=srt)
+            assert np.array_equal(a, b), (N, srt)
+
+
+def test_union_matches_oracle_and_printed_counts(dvl, oracle_mod):
+    A, B = S.union_sets(3, S.V_FULL, 47149, 9749, 9749 - 5606)
+    u = dvl.union_sorted(A, B)
+    assert np.array_equal(u, oracle_mod.union_sorted(A, B))
+    assert u.shape[0] == 52755
+    assert dvl.union_sorted([], []).shape[0] == 0
+    assert list(dvl.union_sorted([3, 1, 3], [2, 1])) == [1, 2, 3]
+
+
+def test_frspec_ranks_from_zipf_stream(dvl, oracle_mod):
+    # the trim list of the 32,768-row workload: top ranks of a Zipf stream
+    tokens = S.zipf_tokens(2, S.V_FULL, 1_000_000)
+    counts = dvl.histogram(tokens, S.V_FULL)
+    ranks = dvl.build_ranks(counts, 32768)
+    assert np.array_equal(ranks, oracle_mod.build_ranks(counts, 32768))
+    assert len(set(ranks.tolist())) == 32768
+    assert np.all(np.diff(counts[ranks]) <= 0)  # rank order
+
+
+def test_host_builder_errors(dvl):
+    with pytest.raises(dvl.DvlError) as e:
+        dvl.histogram(np.array([0, 7], np.int32), 5)
+    assert e.value.status == 2
+    with pytest.raises(dvl.DvlError) as e:
+        dvl.build_ranks(np.zeros(5, np.int64), 3, forced=[9])
+    assert e.value.status == 2
+
+
+def test_ranks_txt_roundtrip(dvl, tmp_path):
+    ids = np.array([5, 0, 248319, 77], np.int32)
+    p = tmp_path / "ranks.txt"
+    dvl.write_ranks_txt(str(p), ids)
+    assert p.read_text() == "5\n0\n248319\n77\n"
+    assert np.array_equal(dvl.read_ranks_txt(str(p)), ids)
+
+
+def _head(**kw):
+    from draft_vocab_lm_gb300._native import DvlHead
+    h = DvlHead()
+    h.dtype, h.N, h.K, h.V = 0, 100, 256, 100
+    h.w = 0x1000
+    for k, v in kw.items():
+        setattr(h, k, v)
+    return h
+
+
+@pytest.mark.parametrize("bad", [
+    dict(dtype=7), dict(N=0), dict(K=100), dict(K=0), dict(K=24576 + 64), dict(reserved=1),
+    dict(w=None), dict(w=0x1004), dict(dtype=1), dict(V=50), dict(id_base=1),
+])
+def test_argument_checks_reject_before_any_launch(dvl, bad):
+    # pointer values are never dereferenced: the checks fail first
+    from draft_vocab_lm_gb300._native import lib
+    L = lib()
+    h = _head(**bad)
+    ids = ctypes.c_void_p(0x2000)
+    st = L.dvl_draft_argmax(ctypes.byref(h), 0x3000, 1, ids, 0x4000, 0x5000, 1 << 20, None)
+    assert st == 1
+
+
+def test_workspace_and_shape_checks(dvl):
+    from draft_vocab_lm_gb300._native import lib
+    L = lib()
+    h = _head()
+    assert L.dvl_draft_argmax(ctypes.byref(h), 0x3000, 0, 0x2000, 0x4000, 0x5000, 1 << 20, None) == 1
+    assert L.dvl_draft_argmax(ctypes.byref(h), 0x3000, 33, 0x2000, 0x4000, 0x5000, 1 << 20, None) == 1
+    assert L.dvl_draft_argmax(ctypes.byref(h), 0x3008, 1, 0x2000, 0x4000, 0x5000, 1 << 20, None) == 1
+    assert L.dvl_draft_argmax(ctypes.byref(h), 0x3000, 1, 0x2000, 0x4000, 0x5000, 100, None) == 4
+    assert L.dvl_draft_argmax(ctypes.byref(h), 0x3000, 1, 0x2000, 0x4000, None, 1 << 20, None) == 4
+    assert L.dvl_draft_topk(ctypes.byref(h), 0x3000, 2, 5, 0x2000, 0x4000, 0x5000, 1 << 20, None) == 1
+    small = _head(N=3)
+    assert L.dvl_draft_topk(ctypes.byref(small), 0x3000, 1, 4, 0x2000, 0x4000, 0x5000, 1 << 20, None) == 1
+    assert L.dvl_draft_topk(ctypes.byref(h), 0x3000, 2, 4, 0x2000, 0x4000, 0x5000, 1000, None) == 4
+
+
+def test_trim_checks_reject_bad_ranks_before_any_launch(dvl):
+    from draft_vocab_lm_gb300._native import lib
+    L = lib()
+    h = _head()
+    ranks = (ctypes.c_int32 * 3)(1, 100, 2)  # 100 is outside [0, V)
+    st = L.dvl_trim_head(ctypes.byref(h), ranks, 3, 0x1000, None, 0x2000, None, None)
+    assert st == 2
+    neg = (ctypes.c_int32 * 1)(-1)
+    assert L.dvl_trim_head(ctypes.byref(h), neg, 1, 0x1000, None, 0x2000, None, None) == 2
+    sliced = _head(N=50)  # not a full head
+    assert L.dvl_trim_head(ctypes.byref(sliced), ranks, 1, 0x1000, None, 0x2000, None, None) == 1
