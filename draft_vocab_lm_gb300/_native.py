@@ -26,7 +26,7 @@ STATUS_NAMES = {
 
 # every symbol include/dvl.h declares
 EXPORTS = (
-    "dvl_status_string", "dvl_version", "dvl_workspace_bytes", "dvl_workspace_init",
+    "dvl_status_string", "dvl_version", "dvl_last_error", "dvl_workspace_bytes", "dvl_workspace_init",
     "dvl_draft_argmax", "dvl_draft_topk", "dvl_trim_head", "dvl_histogram",
     "dvl_build_ranks", "dvl_union_sorted",
 )
@@ -77,6 +77,8 @@ def lib():
         L.dvl_status_string.restype = ctypes.c_char_p
         L.dvl_version.argtypes = []
         L.dvl_version.restype = ctypes.c_int
+        L.dvl_last_error.argtypes = []
+        L.dvl_last_error.restype = ctypes.c_char_p
         L.dvl_workspace_bytes.argtypes = [i32, i32]
         L.dvl_workspace_bytes.restype = sz
         L.dvl_workspace_init.argtypes = [p, sz, p]
@@ -95,4 +97,7 @@ def lib():
 
 def check(fn: str, status: int) -> None:
     if status != 0:
-        raise DvlError(fn, status)
+        err = DvlError(fn, status)
+        if status == 5:
+            err.args = (f"{err.args[0]} ({lib().dvl_last_error().decode()})",)
+        raise err

@@ -19,6 +19,14 @@ namespace {
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_dev;
 std::map<std::tuple<const void *, int, size_t>, int> g_occ;
+std::map<std::pair<const void *, int>, size_t> g_smem_limit;  // per kernel and device
+thread_local cudaError_t t_last_error = cudaSuccess;
+
+dvl_status cuda_failed(cudaError_t e)
+{
+    t_last_error = e;
+    return DVL_ERR_CUDA;
+}
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 }  // namespace
@@ -71,9 +79,18 @@ cudaError_t blocks_per_sm(const void *func, int threads, size_t smem, int *out)
         return e;
     if (smem > (size_t)di.smem_optin)
         return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return e;
+    {
+        // The dynamic shared-memory limit is a property of the kernel, shared
+        // by every launch of it: only ever raise it.
+        std::lock_guard<std::mutex> g(g_mu);
+        size_t &lim = g_smem_limit[std::make_pair(func, dev)];
+        if (smem > lim) {
+            e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess)
+                return e;
+            lim = smem;
+        }
+    }
     int n = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem);
     if (e != cudaSuccess)
@@ -148,7 +165,7 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
         cudaError_t e = hd->dtype == DVL_BF16 ? launch_argmax_bf16(a, mc, kmax, s)
                                               : launch_argmax_nvfp4(a, mc, kmax, s);
         if (e != cudaSuccess)
-            return DVL_ERR_CUDA;
+            return cuda_failed(e);
     }
     return DVL_OK;
 }
@@ -174,7 +191,7 @@ const char *dvl_status_string(int status)
     }
 }
 
-int dvl_version(void) { return 100; }
+int dvl_version(void) { return 101; }
 
 size_t dvl_workspace_bytes(int32_t M, int32_t k)
 {
@@ -190,8 +207,9 @@ dvl_status dvl_workspace_init(void *ws, size_t bytes, void *stream)
 {
     if (!ws || !aligned(ws, 16) || bytes < kWsSlots)
         return DVL_ERR_WORKSPACE;
-    if (cudaMemsetAsync(ws, 0, bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return DVL_ERR_CUDA;
+    cudaError_t e = cudaMemsetAsync(ws, 0, bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_failed(e);
     return DVL_OK;
 }
 
@@ -233,11 +251,11 @@ dvl_status dvl_trim_head(const dvl_head *full, const int32_t *ranks, int32_t n_r
     if (n_duplicates)
         *n_duplicates = dup;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(d2t, ranks, (size_t)n_ranks * sizeof(int32_t), cudaMemcpyHostToDevice, s) !=
-        cudaSuccess)
-        return DVL_ERR_CUDA;
+    cudaError_t e =
+        cudaMemcpyAsync(d2t, ranks, (size_t)n_ranks * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess)
+        return cuda_failed(e);
     const int64_t K = full->K;
-    cudaError_t e;
     if (full->dtype == DVL_BF16) {
         e = launch_trim_rows(static_cast<const unsigned char *>(full->w), K * 2,
                              static_cast<unsigned char *>(w_trim), d2t, n_ranks, s);
@@ -247,7 +265,9 @@ dvl_status dvl_trim_head(const dvl_head *full, const int32_t *ranks, int32_t n_r
         if (e == cudaSuccess)
             e = launch_trim_rows(full->scales, K / 16, scales_trim, d2t, n_ranks, s);
     }
-    return e == cudaSuccess ? DVL_OK : DVL_ERR_CUDA;
+    return e == cudaSuccess ? DVL_OK : cuda_failed(e);
 }
+
+const char *dvl_last_error(void) { return cudaGetErrorString(t_last_error); }
 
 }  // extern "C"

@@ -95,6 +95,10 @@ const char *dvl_status_string(int status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int dvl_version(void);
 
+/* The CUDA runtime's description of the error behind the calling thread's
+ * most recent DVL_ERR_CUDA ("no error" if there was none).  Static storage. */
+const char *dvl_last_error(void);
+
 /* ---------------------------------------------------------------------- */
 /* Workspace                                                              */
 /* ---------------------------------------------------------------------- */
@@ -120,8 +124,9 @@ dvl_status dvl_workspace_init(void *ws, size_t bytes, void *stream);
  * logit sum_k W[n][k] * h[m][k], and that logit.  The dot products run in
  * fp32 on the device (products of bf16 values are exact; the order of the
  * additions is the kernel's).  Exactly equal logits go to the lowest full
- * id; a NaN logit never wins (a row whose every logit is NaN yields id -1
- * and a NaN logit); -0 and +0 compare equal and +0 is reported.  For NVFP4,
+ * id; a NaN logit ranks below every number (among NaN logits the lowest id
+ * wins, reported with a NaN logit); -0 and +0 compare equal and +0 is
+ * reported.  For NVFP4,
  * weight = e2m1(code) * e4m3(scale) * global_scale, and the kernel applies
  * global_scale to the finished dot product.
  *   head:      the head (see dvl_head); host struct, device pointers.

@@ -32,7 +32,8 @@ def test_exports_every_declared_symbol(dvl):
     assert set(declared) == set(_native.EXPORTS)
     for name in declared:
         assert hasattr(lib, name), name
-    assert dvl.version() == 100
+    assert dvl.version() == 101
+    assert lib.dvl_last_error() == b"no error"
     assert lib.dvl_status_string(0) == b"ok"
     assert lib.dvl_status_string(4) == b"workspace missing or too small"
 
