@@ -6,21 +6,25 @@
 // happening" / "Re-running the comparison fairly": the skinny low-M kernel and
 // the local argmax reduction.)
 //
-// Work split.  The grid is persistent (a fixed number of blocks per SM).  The
-// N rows are cut into one contiguous, balanced range per warp of the whole
-// grid.  A warp walks its range RPW rows at a time; for each group of rows
-// every lane reads 16 bytes (8 weights) of each row per 256-wide k step, so
-// one warp load instruction covers 512 contiguous bytes of one row.  The
-// hidden rows sit in shared memory as fp32, laid out so that the lane's 8
-// values for a k step are two conflict-free 16-byte reads; they are read once
-// per k step and reused for the RPW rows.  Loads run NBUF k steps ahead of
-// the arithmetic through a register ring.
+// Work split.  The grid is persistent (two 256-thread blocks per SM).  The N
+// rows are cut into one contiguous, balanced range per warp of the whole grid
+// (+-1 row).  A warp walks its range RPW rows at a time ("a group"); for each
+// group every lane reads 16 bytes (8 weights) of each row per 256-wide k step,
+// so one warp load instruction covers 512 contiguous bytes of one row.  Loads
+// run NB k steps ahead of the arithmetic through a register ring, across group
+// boundaries.  For the hidden widths of the workloads (2,560 and 5,120) K is a
+// compile-time constant: the k loop is fully unrolled and every load of a
+// group is one base pointer plus an immediate offset, so streaming costs one
+// load instruction per 16 bytes and nothing else.  Other widths (multiples
+// of 64) take the same kernel with K read at run time.
 //
-// At the end of a row group the RPW x M partial sums are combined across the
-// warp by a reduce-scatter; the lane that ends up owning (row r, hidden row m)
+// The hidden rows sit in shared memory as fp32, laid out so that the lane's 8
+// values for a k step are two conflict-free 16-byte reads, reused for the RPW
+// rows.  At the end of a group the RPW x M partial sums are combined across
+// the warp by a reduce-scatter; the lane that ends up owning (row, hidden row)
 // forms the packed key (logit, full id) and keeps its best keys.  Each block
-// then merges its lanes' lists and the last block to finish merges the grid's
-// (see block_finish).
+// then merges its lanes' lists and the last block to finish merges the
+// grid's (block_finish).
 #include <cuda_runtime.h>
 
 #include "dvl_device.cuh"
@@ -30,40 +34,56 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRPW = 4;        // rows a warp works on together
-constexpr int kNBuf = 2;       // k steps of loads in flight per lane
 constexpr int kKStep = 256;    // weights per row per warp load instruction
-static_assert(kWarps * kRPW == 32, "block_finish expects 32 lists per hidden row");
 
-// Shared-memory offset (in floats) of hidden element e of row m: element
-// e = 256 j + 8 l + 4 half + i sits at m*Kpad + 256 j + 128 half + 4 l + i.
+// Shared-memory offset (in floats) of hidden element e of a row: element
+// e = 256 j + 8 l + 4 half + i sits at 256 j + 128 half + 4 l + i.
 __device__ __forceinline__ int h_slot(int e)
 {
     return (e & ~255) + ((e & 4) << 5) + ((e & 255) >> 3) * 4 + (e & 3);
 }
 
-template <int M>
-__device__ __forceinline__ void fma8(float &s, const uint4 &w, const float4 &h0, const float4 &h1)
+template <int RPW, int M>
+__device__ __forceinline__ void fma_step(float (&acc)[RPW][M], const uint4 (&w)[RPW],
+                                         const float *hp, int Kpad)
 {
-    s = fmaf(bf16_lo(w.x), h0.x, s);
-    s = fmaf(bf16_hi(w.x), h0.y, s);
-    s = fmaf(bf16_lo(w.y), h0.z, s);
-    s = fmaf(bf16_hi(w.y), h0.w, s);
-    s = fmaf(bf16_lo(w.z), h1.x, s);
-    s = fmaf(bf16_hi(w.z), h1.y, s);
-    s = fmaf(bf16_lo(w.w), h1.z, s);
-    s = fmaf(bf16_hi(w.w), h1.w, s);
+    float wf[RPW][8];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        wf[r][0] = bf16_lo(w[r].x); wf[r][1] = bf16_hi(w[r].x);
+        wf[r][2] = bf16_lo(w[r].y); wf[r][3] = bf16_hi(w[r].y);
+        wf[r][4] = bf16_lo(w[r].z); wf[r][5] = bf16_hi(w[r].z);
+        wf[r][6] = bf16_lo(w[r].w); wf[r][7] = bf16_hi(w[r].w);
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const float4 h0 = *reinterpret_cast<const float4 *>(hp + m * Kpad);
+        const float4 h1 = *reinterpret_cast<const float4 *>(hp + m * Kpad + 128);
+        const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            float s = acc[r][m];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                s = fmaf(wf[r][e], hv[e], s);
+            acc[r][m] = s;
+        }
+    }
 }
 
-template <int M, int KM>
+// K == KC (a multiple of 256) when KC > 0; K read from the arguments when 0.
+template <int M, int KM, int KC, int NB, int RPW>
 __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxArgs a)
 {
+    constexpr int kLists = kWarps * RPW;
     extern __shared__ __align__(16) unsigned char smem[];
+    const int K = KC > 0 ? KC : a.K;
+    const int Kpad = KC > 0 ? KC : a.Kpad;
+    const int J = Kpad / kKStep;
     float *s_h = reinterpret_cast<float *>(smem);                       // [M][Kpad]
-    uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + (size_t)M * a.Kpad * 4);
+    uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + (size_t)M * Kpad * 4);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int K = a.K, Kpad = a.Kpad, J = Kpad / kKStep;
     const uint16_t *__restrict__ W = static_cast<const uint16_t *>(a.w);
 
     // Stage the hidden rows (bf16 -> fp32, zero past K).
@@ -77,6 +97,8 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
         dst[0] = bf16_lo(x);
         dst[1] = bf16_hi(x);
     }
+    for (int i = tid; i < M * kLists * KM; i += kThreads)
+        s_cand[i] = 0ull;
     __syncthreads();
 
     // This warp's rows.
@@ -84,11 +106,10 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
     const long long gw = (long long)blockIdx.x * kWarps + warp;
     const int row0 = (int)((long long)a.N * gw / GW);
     const int nrows = (int)((long long)a.N * (gw + 1) / GW) - row0;
-    const int nsteps = (nrows + kRPW - 1) / kRPW;
-    const int total = nsteps * J;
+    const int ngroups = (nrows + RPW - 1) / RPW;
 
     // Which (row slot, hidden row) this lane owns after the reduce-scatter.
-    constexpr int NV = kRPW * M;
+    constexpr int NV = RPW * M;
     constexpr int P = pow2_ceil(NV);
     constexpr int SH = 5 - log2_exact(P);
     const int vi = lane >> SH;
@@ -97,109 +118,151 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
 
     TopList<KM> best;
     best.init();
-    float acc[kRPW][M];
+    float acc[RPW][M];
 #pragma unroll
-    for (int r = 0; r < kRPW; ++r)
+    for (int r = 0; r < RPW; ++r)
 #pragma unroll
         for (int m = 0; m < M; ++m)
             acc[r][m] = 0.f;
 
-    const uint16_t *wlane = W + 8 * lane;
-    const bool ktail = (K % kKStep) != 0;
-    int ls = 0, lj = 0;           // load cursor (row group, k step)
-    int cs = 0, cj = 0;           // consume cursor
-    int pend_id = 0;
-
-    uint4 buf[kNBuf][kRPW];
-
-    auto issue = [&](uint4(&b)[kRPW]) {
-        const bool kin = !ktail || (lj * kKStep + 8 * lane) < K;
-        const uint16_t *p = wlane + (size_t)(row0 + ls * kRPW) * K + lj * kKStep;
+    auto finish_group = [&](int g, int pend_id) {
+        float v[P];
 #pragma unroll
-        for (int r = 0; r < kRPW; ++r) {
-            if (kin && ls * kRPW + r < nrows)
-                b[r] = ld_stream16(p + (size_t)r * K);
-            else
-                b[r] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (++lj == J) {
-            lj = 0;
-            ++ls;
-        }
-    };
-
-    auto consume = [&](const uint4(&b)[kRPW]) {
-        if (cj == 0 && owner) {
-            const int rr = cs * kRPW + own_r;
-            if (rr < nrows) {
-                const int row = row0 + rr;
-                pend_id = a.d2t ? __ldg(a.d2t + row) : (int)(a.id_base + row);
+        for (int i = 0; i < P; ++i)
+            v[i] = 0.f;
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                v[r * M + m] = acc[r][m];
+                acc[r][m] = 0.f;
             }
+        warp_reduce_scatter<P>(v);
+        if (owner && g * RPW + own_r < nrows)
+            best.insert(make_key(v[0], pend_id));
+    };
+    auto owner_id = [&](int g) {
+        int id = 0;
+        const int rr = g * RPW + own_r;
+        if (owner && rr < nrows) {
+            const int row = row0 + rr;
+            id = a.d2t ? __ldg(a.d2t + row) : (int)(a.id_base + row);
         }
-        const float *hp = s_h + cj * kKStep + lane * 4;
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-            const float4 h0 = *reinterpret_cast<const float4 *>(hp + m * Kpad);
-            const float4 h1 = *reinterpret_cast<const float4 *>(hp + m * Kpad + 128);
-#pragma unroll
-            for (int r = 0; r < kRPW; ++r)
-                fma8<M>(acc[r][m], b[r], h0, h1);
-        }
-        if (++cj == J) {
-            float v[P];
-#pragma unroll
-            for (int i = 0; i < P; ++i)
-                v[i] = 0.f;
-#pragma unroll
-            for (int r = 0; r < kRPW; ++r)
-#pragma unroll
-                for (int m = 0; m < M; ++m) {
-                    v[r * M + m] = acc[r][m];
-                    acc[r][m] = 0.f;
-                }
-            warp_reduce_scatter<P>(v);
-            if (owner && cs * kRPW + own_r < nrows)
-                best.insert(make_key(v[0], pend_id));
-            cj = 0;
-            ++cs;
-        }
+        return id;
     };
 
+    if constexpr (KC > 0) {
+        // ---- compile-time K: unrolled k loop, immediate-offset loads ----
+        constexpr int JC = KC / kKStep;
+        static_assert(JC % NB == 0, "the ring must divide the k steps");
+        const uint16_t *gp = W + (size_t)row0 * KC + 8 * lane;
+        uint4 buf[NB][RPW];
 #pragma unroll
-    for (int b = 0; b < kNBuf; ++b)
-        issue(buf[b]);
-    for (int t0 = 0; t0 < total; t0 += kNBuf) {
+        for (int j = 0; j < NB; ++j)
 #pragma unroll
-        for (int b = 0; b < kNBuf; ++b) {
-            if (t0 + b < total)
-                consume(buf[b]);
+            for (int r = 0; r < RPW; ++r)
+                buf[j][r] = make_uint4(0u, 0u, 0u, 0u);
+        bool vcur[RPW];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+            vcur[r] = r < nrows;
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+                if (vcur[r])
+                    buf[j][r] = __ldg(reinterpret_cast<const uint4 *>(gp + r * KC + j * kKStep));
+        for (int g = 0; g < ngroups; ++g) {
+            bool vnext[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+                vnext[r] = (g + 1) * RPW + r < nrows;
+            const int pend_id = owner_id(g);
+            const float *hp = s_h + lane * 4;
+#pragma unroll
+            for (int j = 0; j < JC; ++j) {
+                const int b = j % NB;
+                fma_step<RPW, M>(acc, buf[b], hp + j * kKStep, KC);
+                const int jj = j + NB;
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    if (jj < JC) {
+                        if (vcur[r])
+                            buf[b][r] = __ldg(
+                                reinterpret_cast<const uint4 *>(gp + r * KC + jj * kKStep));
+                    } else if (vnext[r]) {
+                        buf[b][r] = __ldg(reinterpret_cast<const uint4 *>(
+                            gp + (RPW + r) * KC + (jj - JC) * kKStep));
+                    }
+                }
+            }
+            finish_group(g, pend_id);
+            gp += RPW * KC;
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+                vcur[r] = vnext[r];
+        }
+    } else {
+        // ---- run-time K: one flat (group, k step) stream, predicated ----
+        constexpr int NBG = 2;
+        const int total = ngroups * J;
+        const uint16_t *wlane = W + 8 * lane;
+        const bool ktail = (K % kKStep) != 0;
+        int ls = 0, lj = 0, cs = 0, cj = 0, pend_id = 0;
+        uint4 buf[NBG][RPW];
+        auto issue = [&](uint4(&b)[RPW]) {
+            const bool kin = !ktail || (lj * kKStep + 8 * lane) < K;
+            const uint16_t *p = wlane + (size_t)(row0 + ls * RPW) * K + lj * kKStep;
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+                b[r] = (kin && ls * RPW + r < nrows) ? ld_stream16(p + (size_t)r * K)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
+            if (++lj == J) {
+                lj = 0;
+                ++ls;
+            }
+        };
+#pragma unroll
+        for (int b = 0; b < NBG; ++b)
             issue(buf[b]);
+        for (int t0 = 0; t0 < total; t0 += NBG) {
+#pragma unroll
+            for (int b = 0; b < NBG; ++b) {
+                if (t0 + b < total) {
+                    if (cj == 0)
+                        pend_id = owner_id(cs);
+                    fma_step<RPW, M>(acc, buf[b], s_h + cj * kKStep + lane * 4, Kpad);
+                    if (++cj == J) {
+                        finish_group(cs, pend_id);
+                        cj = 0;
+                        ++cs;
+                    }
+                }
+                issue(buf[b]);
+            }
         }
     }
 
-    // Block merge input: 32 lists per hidden row (one per warp x row slot).
-    for (int i = tid; i < M * 32 * KM; i += kThreads)
-        s_cand[i] = 0ull;
-    __syncthreads();
     if (owner) {
 #pragma unroll
         for (int i = 0; i < KM; ++i)
-            s_cand[(own_m * 32 + warp * kRPW + own_r) * KM + i] = best.v[i];
+            s_cand[(own_m * kLists + warp * RPW + own_r) * KM + i] = best.v[i];
     }
     __syncthreads();
-    block_finish<KM>(s_cand, M, a);
+    block_finish<KM>(s_cand, M, kLists, a);
 }
 
-template <int M, int KM>
-cudaError_t launch_one(const ArgmaxArgs &a, cudaStream_t s)
+template <int M, int KM, int KC, int NB, int RPW>
+cudaError_t launch_cfg(const ArgmaxArgs &a, cudaStream_t s)
 {
-    const size_t smem = (size_t)M * a.Kpad * 4 + (size_t)M * 32 * KM * 8;
+    const size_t smem = (size_t)M * a.Kpad * 4 + (size_t)M * kWarps * RPW * KM * 8;
     DeviceInfo di;
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess)
         return e;
+    auto kern = argmax_bf16_kernel<M, KM, KC, NB, RPW>;
     int per_sm = 0;
-    e = blocks_per_sm(reinterpret_cast<const void *>(argmax_bf16_kernel<M, KM>), kThreads, smem, &per_sm);
+    e = blocks_per_sm(reinterpret_cast<const void *>(kern), kThreads, smem, &per_sm);
     if (e != cudaSuccess)
         return e;
     if (per_sm < 1)
@@ -207,30 +270,42 @@ cudaError_t launch_one(const ArgmaxArgs &a, cudaStream_t s)
     if (per_sm > 2)
         per_sm = 2;
     long long grid = (long long)di.sms * per_sm;
-    // at least one row per warp
-    const long long max_by_rows = ((long long)a.N + kWarps - 1) / kWarps;
+    const long long max_by_rows = ((long long)a.N + kWarps - 1) / kWarps;  // >= 1 row per warp
     if (grid > max_by_rows)
         grid = max_by_rows;
     if (grid > kMaxCtas)
         grid = kMaxCtas;
     if (grid < 1)
         grid = 1;
-    argmax_bf16_kernel<M, KM><<<(unsigned)grid, kThreads, smem, s>>>(a);
+    kern<<<(unsigned)grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
+}
+
+// Per hidden-row count: ring depth and rows per group for each width.
+template <int M, int KM>
+cudaError_t launch_m(const ArgmaxArgs &a, cudaStream_t s)
+{
+    // deeper rings where the registers allow it (no spills at 128 per thread)
+    constexpr int NB = M <= 2 ? 5 : 2;
+    if (a.K == 2560)
+        return launch_cfg<M, KM, 2560, NB, 4>(a, s);
+    if (a.K == 5120)
+        return launch_cfg<M, KM, 5120, NB, 4>(a, s);
+    return launch_cfg<M, KM, 0, 2, 4>(a, s);
 }
 
 template <int KM>
 cudaError_t dispatch_m(const ArgmaxArgs &a, int M, cudaStream_t s)
 {
     switch (M) {
-    case 1: return launch_one<1, KM>(a, s);
-    case 2: return launch_one<2, KM>(a, s);
-    case 3: return launch_one<3, KM>(a, s);
-    case 4: return launch_one<4, KM>(a, s);
-    case 5: return launch_one<5, KM>(a, s);
-    case 6: return launch_one<6, KM>(a, s);
-    case 7: return launch_one<7, KM>(a, s);
-    case 8: return launch_one<8, KM>(a, s);
+    case 1: return launch_m<1, KM>(a, s);
+    case 2: return launch_m<2, KM>(a, s);
+    case 3: return launch_m<3, KM>(a, s);
+    case 4: return launch_m<4, KM>(a, s);
+    case 5: return launch_m<5, KM>(a, s);
+    case 6: return launch_m<6, KM>(a, s);
+    case 7: return launch_m<7, KM>(a, s);
+    case 8: return launch_m<8, KM>(a, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
             s_cand[(own_m * 32 + warp * kRPW + own_r) * KM + i] = best.v[i];
     }
     __syncthreads();
-    block_finish<KM>(s_cand, M, a);
+    block_finish<KM>(s_cand, M, 32, a);
 }
 
 template <int M, int KM>

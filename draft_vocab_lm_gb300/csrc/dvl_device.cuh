@@ -145,7 +145,8 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[P])
 
 // Cross-block finish of a reducing kernel.  Every block calls it once, after
 // its own candidates are final, with s_cand holding, for each of the M rows,
-// 32 lane lists of KM keys ([M][32][KM] in shared memory).
+// `nlists` lists of KM keys ([M][nlists][KM] in shared memory; nlists is a
+// multiple of 32, lane l of the merging warp takes lists l, l + 32, ...).
 //  - k == 1: the block's best key per row goes to the workspace with a 64-bit
 //    atomicMax; the last block to finish swaps each key back to 0 and writes
 //    the id and the logit.
@@ -155,7 +156,8 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[P])
 // gridDim.x - 1), so the ticket is 0 again when the call ends.  No block
 // waits for another.
 template <int KM>
-__device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, const ArgmaxArgs &a)
+__device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int nlists,
+                                             const ArgmaxArgs &a)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
@@ -166,9 +168,11 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, cons
 
     for (int m = warp; m < M; m += nwarps) {
         TopList<KM> L;
+        L.init();
+        for (int l = lane; l < nlists; l += 32)
 #pragma unroll
-        for (int i = 0; i < KM; ++i)
-            L.v[i] = s_cand[(m * 32 + lane) * KM + i];
+            for (int i = 0; i < KM; ++i)
+                L.insert(s_cand[(m * nlists + l) * KM + i]);
         if (KM == 1) {
             uint64_t key = warp_max_u64(L.v[0]);
             if (lane == 0 && key != 0ull)
