@@ -27,7 +27,8 @@ STATUS_NAMES = {
 # every symbol include/dvl.h declares
 EXPORTS = (
     "dvl_status_string", "dvl_version", "dvl_last_error", "dvl_workspace_bytes", "dvl_workspace_init",
-    "dvl_draft_argmax", "dvl_draft_topk", "dvl_trim_head", "dvl_histogram",
+    "dvl_draft_argmax", "dvl_draft_topk", "dvl_draft_argmax_noalloc", "dvl_trim_head",
+    "dvl_histogram",
     "dvl_build_ranks", "dvl_union_sorted",
 )
 

@@ -171,6 +171,20 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
 }
 
 }  // namespace
+
+dvl_status check_reduce_args(const dvl_head *hd, const void *h, int32_t M, int32_t k,
+                             const void *ids, const void *logits)
+{
+    dvl_status st = check_head(hd);
+    if (st != DVL_OK)
+        return st;
+    if (M < 1 || M > DVL_MAX_M || k < 1 || k > DVL_MAX_TOPK || k > hd->N)
+        return DVL_ERR_INVALID_ARG;
+    if (!h || !aligned(h, 16) || !ids || !aligned(ids, 4) || !logits || !aligned(logits, 4))
+        return DVL_ERR_INVALID_ARG;
+    return DVL_OK;
+}
+
 }  // namespace dvl
 
 using namespace dvl;

@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+#include "dvl.h"
+
 namespace dvl {
 
 // Workspace layout (device bytes).  Every kernel call leaves it as it found
@@ -50,6 +52,10 @@ cudaError_t launch_argmax_bf16(const ArgmaxArgs &a, int M, int kmax, cudaStream_
 cudaError_t launch_argmax_nvfp4(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
 int max_chunk_rows_bf16(int K);
 int max_chunk_rows_nvfp4(int K);
+
+// The argument checks of draft_argmax / draft_topk, without the workspace.
+dvl_status check_reduce_args(const dvl_head *hd, const void *h, int32_t M, int32_t k,
+                             const void *ids, const void *logits);
 
 cudaError_t launch_trim_rows(const unsigned char *src, int64_t src_row_bytes,
                              unsigned char *dst, const int32_t *ranks, int n,

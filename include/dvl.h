@@ -156,6 +156,31 @@ dvl_status dvl_draft_topk(const dvl_head *head, const void *h, int32_t M, int32_
                           int32_t *ids, float *logits, void *ws, size_t ws_bytes,
                           void *stream);
 
+/* dvl_draft_argmax for callers that cannot allocate device memory.  The
+ * pages have no counterpart of this entry point.
+ *
+ * Who needs it: code running as a plugin inside an inference engine that
+ * owns every device allocation (raw cudaMalloc is not available to it), and
+ * latency-critical decode loops where a cudaMalloc would stall the pipeline
+ * (it may synchronize the device).  Such a caller passes the head, h and the
+ * outputs only; the reduction scratch lives in a fixed 512-byte array in the
+ * library's own device memory (a static __device__ array: every GPU that
+ * loads the library keeps it until the process exits).  This entry point
+ * allocates nothing and frees nothing.
+ *   Same arguments, arithmetic, results and errors as dvl_draft_argmax,
+ *   without ws / ws_bytes.  M above DVL_MAX_M (32), the most the fixed
+ *   scratch holds, returns DVL_ERR_INVALID_ARG before anything is enqueued.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, once per device, with that device current); make
+ *   that first call before any stream capture.
+ *   Every call clears the scratch with a memset enqueued on `stream`, then
+ *   runs the argmax on it.  All calls on a device share the one array: two
+ *   calls that may run at the same time on the GPU (on different streams, or
+ *   from different threads) race on it and may return wrong results.  Keep
+ *   them in one stream order. */
+dvl_status dvl_draft_argmax_noalloc(const dvl_head *head, const void *h, int32_t M,
+                                    int32_t *ids, float *max_logit, void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* Load time                                                              */
 /* ---------------------------------------------------------------------- */
