@@ -286,7 +286,7 @@ def run_ours(args):
 
     # ---- the headline: full-vocab bf16 head, M = 1, argmax -------------------
     wl2 = S.c2(Ms=(1, 3))
-    head2 = dvl.Head(dev(torch, wl2.w), V=wl2.V)
+    head2 = dvl.Head(dev(torch, wl2.w), V=wl2.V, static=True)
     N2, K2 = wl2.N, wl2.K
     ws = dvl.make_workspace(32, 4)
     h1 = dev(torch, wl2.h[1])
@@ -437,8 +437,9 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
     del wf
     b1 = RL.call_bytes(wl1.N, wl1.K, 1)
     R1 = rotation_copies(b1, l2)
-    heads = [dvl.Head(w_trim.clone() if r else w_trim, V=wl1.V, d2t=d2t1.clone() if r else d2t1)
-             for r in range(R1)]
+    torch.cuda.synchronize()  # the trimmed head is complete: static from here on
+    heads = [dvl.Head(w_trim.clone() if r else w_trim, V=wl1.V, d2t=d2t1.clone() if r else d2t1,
+                      static=True) for r in range(R1)]
     h1s = dev(torch, wl1.h[1])
     t = repeat_stats(torch, lambda i: dvl.draft_argmax(heads[i % R1], h1s, ids=ids, logits=lg,
                                                        ws=ws), n_calls, R)
@@ -450,6 +451,11 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
     t = repeat_stats(torch, lambda i: gsl.replay(), 4, R)
     out["c1_shortlist16k_M1_argmax_graph50"] = entry(b1, t[0] / 50, t[1] / 50, t[2] / 50, peak,
                                                      {"l2_rotation_copies": R1})
+    h3s = dev(torch, S.hidden_bf16(3, 3, wl1.K))
+    t = repeat_stats(torch, lambda i: dvl.draft_argmax(heads[i % R1], h3s, ids=ids, logits=lg,
+                                                       ws=ws), n_calls, R)
+    out["c1_shortlist16k_M3_argmax"] = entry(RL.call_bytes(wl1.N, wl1.K, 3), *t, peak,
+                                             {"l2_rotation_copies": R1})
     t_hot = repeat_stats(torch, lambda i: dvl.draft_argmax(heads[0], h1s, ids=ids, logits=lg,
                                                            ws=ws), n_calls, R)
     out["c1_shortlist16k_M1_argmax_l2hot"] = entry(b1, *t_hot, peak, {"note": "L2-hot, same copy"})
@@ -466,7 +472,9 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
     del wf
     b3 = RL.call_bytes(len(ranks), wl3.K, 1)
     R3 = rotation_copies(b3, l2)
-    heads3 = [dvl.Head(w_trim3.clone() if r else w_trim3, V=wl3.V, d2t=d2t3) for r in range(R3)]
+    torch.cuda.synchronize()
+    heads3 = [dvl.Head(w_trim3.clone() if r else w_trim3, V=wl3.V, d2t=d2t3, static=True)
+              for r in range(R3)]
     for M in wl3.Ms:
         hh = dev(torch, wl3.h[M])
         t = repeat_stats(torch, lambda i: dvl.draft_argmax(heads3[i % R3], hh, ids=ids, logits=lg,
@@ -481,7 +489,8 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
         W = dev(torch, wl4.extra["w_by_M"][M])
         b4 = RL.call_bytes(wl4.N, wl4.K, M)
         R4 = rotation_copies(b4, l2)
-        hs = [dvl.Head(W.clone() if r else W, V=wl4.V, d2t=d2t4) for r in range(R4)]
+        torch.cuda.synchronize()
+        hs = [dvl.Head(W.clone() if r else W, V=wl4.V, d2t=d2t4, static=True) for r in range(R4)]
         hh = dev(torch, wl4.h[M])
         t = repeat_stats(torch, lambda i: dvl.draft_argmax(hs[i % R4], hh, ids=ids, logits=lg,
                                                            ws=ws), 50, R)
@@ -496,8 +505,9 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
     d2t5 = dev(torch, wl5.d2t)
     b5 = RL.call_bytes(wl5.N, wl5.K, 1, dtype="nvfp4")
     R5 = rotation_copies(b5, l2)
+    torch.cuda.synchronize()
     hs = [dvl.Head(q.clone() if r else q, scales=sc.clone() if r else sc, global_scale=wl5.g,
-                   V=wl5.V, d2t=d2t5) for r in range(R5)]
+                   V=wl5.V, d2t=d2t5, static=True) for r in range(R5)]
     for M in wl5.Ms:
         hh = dev(torch, wl5.h[M])
         t = repeat_stats(torch, lambda i: dvl.draft_argmax(hs[i % R5], hh, ids=ids, logits=lg,

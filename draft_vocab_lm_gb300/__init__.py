@@ -22,8 +22,8 @@ import ctypes
 import numpy as np
 
 from . import roofline
-from ._native import (DVL_BF16, DVL_K_MULTIPLE, DVL_MAX_K, DVL_MAX_M, DVL_MAX_TOPK,
-                      DVL_NVFP4, DvlError, DvlHead, check, lib)
+from ._native import (DVL_BF16, DVL_HEAD_STATIC, DVL_K_MULTIPLE, DVL_MAX_K, DVL_MAX_M,
+                      DVL_MAX_TOPK, DVL_NVFP4, DvlError, DvlHead, check, lib)
 
 __all__ = [
     "Head", "DvlError", "draft_argmax", "draft_topk", "trim_head", "workspace_bytes",
@@ -58,10 +58,15 @@ class Head:
               shifted by id_base).
     scales:   NVFP4 only: uint8 E4M3 [N][K/16].
     global_scale: NVFP4 tensor scale.
+    static:   promise that no work still pending on the stream writes w,
+              scales or d2t when a call is enqueued (weights loaded earlier;
+              not a head trim_head has just filled on the same stream).  The
+              kernel may then start streaming the head while the preceding
+              kernel on the stream finishes.
     """
 
     def __init__(self, w, *, V: int | None = None, d2t=None, scales=None,
-                 global_scale: float = 1.0, id_base: int = 0):
+                 global_scale: float = 1.0, id_base: int = 0, static: bool = False):
         torch = _torch()
         if not w.is_cuda or w.dim() != 2 or not w.is_contiguous():
             raise ValueError("w must be a contiguous 2-D CUDA tensor")
@@ -89,9 +94,16 @@ class Head:
                     or tuple(d2t.shape) != (self.N,)):
                 raise ValueError("d2t must be a contiguous CUDA int32 [N] tensor")
         self.d2t = d2t
+        self.static = bool(static)
         self.device = w.device
+        self._struct = None
 
     def struct(self) -> DvlHead:
+        if self._struct is None:
+            self._struct = self._make_struct()
+        return self._struct
+
+    def _make_struct(self) -> DvlHead:
         s = DvlHead()
         s.dtype = self.dtype
         s.N = self.N
@@ -102,6 +114,7 @@ class Head:
         s.scales = self.scales.data_ptr() if self.scales is not None else None
         s.global_scale = self.global_scale
         s.d2t = self.d2t.data_ptr() if self.d2t is not None else None
+        s.flags = DVL_HEAD_STATIC if self.static else 0
         return s
 
     def slice_rows(self, n0: int, n1: int) -> "Head":
@@ -114,6 +127,7 @@ class Head:
         h.d2t = self.d2t[n0:n1] if self.d2t is not None else None
         h.id_base = self.id_base + (n0 if self.d2t is None else 0)
         h.N = n1 - n0
+        h._struct = None
         return h
 
 
@@ -156,9 +170,8 @@ def draft_topk(head: Head, h, k: int, *, ids=None, logits=None, ws=None, stream=
         logits = torch.empty((M, k), dtype=torch.float32, device=h.device)
     if ws is None:
         ws = make_workspace(M, k, device=h.device, stream=stream)
-    st = head.struct()
     check("dvl_draft_topk",
-          lib().dvl_draft_topk(ctypes.byref(st), h.data_ptr(), M, int(k), ids.data_ptr(),
+          lib().dvl_draft_topk(ctypes.byref(head.struct()), h.data_ptr(), M, int(k), ids.data_ptr(),
                                logits.data_ptr(), ws.data_ptr(), ws.numel(),
                                _stream_handle(stream, h.device)))
     return ids, logits
@@ -175,9 +188,8 @@ def draft_argmax(head: Head, h, *, ids=None, logits=None, ws=None, stream=None):
         logits = torch.empty(M, dtype=torch.float32, device=h.device)
     if ws is None:
         ws = make_workspace(M, 1, device=h.device, stream=stream)
-    st = head.struct()
     check("dvl_draft_argmax",
-          lib().dvl_draft_argmax(ctypes.byref(st), h.data_ptr(), M, ids.data_ptr(),
+          lib().dvl_draft_argmax(ctypes.byref(head.struct()), h.data_ptr(), M, ids.data_ptr(),
                                  logits.data_ptr(), ws.data_ptr(), ws.numel(),
                                  _stream_handle(stream, h.device)))
     return ids, logits

@@ -17,6 +17,7 @@ DVL_MAX_M = 32
 DVL_MAX_TOPK = 4
 DVL_K_MULTIPLE = 64
 DVL_MAX_K = 24576
+DVL_HEAD_STATIC = 1
 
 STATUS_NAMES = {
     0: "DVL_OK", 1: "DVL_ERR_INVALID_ARG", 2: "DVL_ERR_OUT_OF_RANGE",
@@ -38,7 +39,7 @@ class DvlHead(ctypes.Structure):
         ("dtype", ctypes.c_int32),
         ("N", ctypes.c_int32),
         ("K", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
         ("V", ctypes.c_int64),
         ("id_base", ctypes.c_int64),
         ("w", ctypes.c_void_p),

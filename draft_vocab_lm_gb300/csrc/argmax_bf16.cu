@@ -36,12 +36,9 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kKStep = 256;    // weights per row per warp load instruction
 
-// Shared-memory offset (in floats) of hidden element e of a row: element
-// e = 256 j + 8 l + 4 half + i sits at 256 j + 128 half + 4 l + i.
-__device__ __forceinline__ int h_slot(int e)
-{
-    return (e & ~255) + ((e & 4) << 5) + ((e & 255) >> 3) * 4 + (e & 3);
-}
+// Shared-memory layout of a hidden row (fp32): element e = 256 j + 8 l +
+// 4 half + i sits at 256 j + 128 half + 4 l + i, so lane l's 8 values for
+// k step j are two conflict-free 16-byte reads.
 
 template <int RPW, int M>
 __device__ __forceinline__ void fma_step(float (&acc)[RPW][M], const uint4 (&w)[RPW],
@@ -86,20 +83,10 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint16_t *__restrict__ W = static_cast<const uint16_t *>(a.w);
 
-    // Stage the hidden rows (bf16 -> fp32, zero past K).
-    for (int i = tid; i < M * (Kpad / 2); i += kThreads) {
-        const int m = i / (Kpad / 2);
-        const int e = 2 * (i - m * (Kpad / 2));
-        uint32_t x = 0u;
-        if (e < K)
-            x = __ldg(reinterpret_cast<const uint32_t *>(a.h + (size_t)m * K + e));
-        float *dst = s_h + m * Kpad + h_slot(e);
-        dst[0] = bf16_lo(x);
-        dst[1] = bf16_hi(x);
-    }
-    for (int i = tid; i < M * kLists * KM; i += kThreads)
-        s_cand[i] = 0ull;
-    __syncthreads();
+    // Let the next kernel on the stream start launching its blocks as soon as
+    // SMs free up (programmatic dependent launch); it waits for this grid's
+    // results before it reads anything this grid writes.
+    pdl_launch_dependents();
 
     // This warp's rows.
     const long long GW = (long long)gridDim.x * kWarps;
@@ -107,6 +94,86 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
     const int row0 = (int)((long long)a.N * gw / GW);
     const int nrows = (int)((long long)a.N * (gw + 1) / GW) - row0;
     const int ngroups = (nrows + RPW - 1) / RPW;
+
+    // The compile-time-K register ring and its first NB k steps.  A head the
+    // caller marked static starts streaming before the wait for the
+    // preceding kernel on the stream; otherwise after it.
+    constexpr int NBc = KC > 0 ? NB : 1;
+    uint4 buf[NBc][RPW];
+#pragma unroll
+    for (int j = 0; j < NBc; ++j)
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+            buf[j][r] = make_uint4(0u, 0u, 0u, 0u);
+    bool vcur[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+        vcur[r] = r < nrows;
+    const uint16_t *gp = W + (size_t)row0 * (KC > 0 ? KC : 0) + 8 * lane;
+    auto prologue = [&]() {
+        if constexpr (KC > 0) {
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+#pragma unroll
+                for (int r = 0; r < RPW; ++r)
+                    if (vcur[r])
+                        buf[j][r] =
+                            __ldg(reinterpret_cast<const uint4 *>(gp + r * KC + j * kKStep));
+        }
+    };
+    if (a.head_static)
+        prologue();
+    // From here on: inputs and workspace that earlier work may have written.
+    pdl_wait();
+
+    // Stage the hidden rows (bf16 -> fp32, zero past K): 16-byte loads, all
+    // of a thread's loads issued before its shared-memory stores.
+    {
+        constexpr int kMaxPer = 8;  // covers M * Kpad <= 8 * 8 * 256 elements
+        const int nvec = M * (Kpad / 8);
+        uint4 v[kMaxPer];
+#pragma unroll
+        for (int u = 0; u < kMaxPer; ++u) {
+            const int i = tid + u * kThreads;
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < nvec) {
+                const int m = i / (Kpad / 8);
+                const int e = 8 * (i - m * (Kpad / 8));
+                if (e < K)
+                    v[u] = __ldg(reinterpret_cast<const uint4 *>(a.h + (size_t)m * K + e));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kMaxPer; ++u) {
+            const int i = tid + u * kThreads;
+            if (i < nvec) {
+                const int m = i / (Kpad / 8);
+                const int e = 8 * (i - m * (Kpad / 8));
+                float *dst = s_h + m * Kpad + (e & ~255) + ((e & 255) >> 3) * 4;
+                *reinterpret_cast<float4 *>(dst) =
+                    make_float4(bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y));
+                *reinterpret_cast<float4 *>(dst + 128) =
+                    make_float4(bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w));
+            }
+        }
+        for (int i = tid + kMaxPer * kThreads; i < nvec; i += kThreads) {
+            const int m = i / (Kpad / 8);
+            const int e = 8 * (i - m * (Kpad / 8));
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (e < K)
+                x = __ldg(reinterpret_cast<const uint4 *>(a.h + (size_t)m * K + e));
+            float *dst = s_h + m * Kpad + (e & ~255) + ((e & 255) >> 3) * 4;
+            *reinterpret_cast<float4 *>(dst) =
+                make_float4(bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y));
+            *reinterpret_cast<float4 *>(dst + 128) =
+                make_float4(bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w));
+        }
+    }
+    for (int i = tid; i < M * kLists * KM; i += kThreads)
+        s_cand[i] = 0ull;
+    __syncthreads();
+    if (!a.head_static)
+        prologue();
 
     // Which (row slot, hidden row) this lane owns after the reduce-scatter.
     constexpr int NV = RPW * M;
@@ -155,23 +222,6 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
         // ---- compile-time K: unrolled k loop, immediate-offset loads ----
         constexpr int JC = KC / kKStep;
         static_assert(JC % NB == 0, "the ring must divide the k steps");
-        const uint16_t *gp = W + (size_t)row0 * KC + 8 * lane;
-        uint4 buf[NB][RPW];
-#pragma unroll
-        for (int j = 0; j < NB; ++j)
-#pragma unroll
-            for (int r = 0; r < RPW; ++r)
-                buf[j][r] = make_uint4(0u, 0u, 0u, 0u);
-        bool vcur[RPW];
-#pragma unroll
-        for (int r = 0; r < RPW; ++r)
-            vcur[r] = r < nrows;
-#pragma unroll
-        for (int j = 0; j < NB; ++j)
-#pragma unroll
-            for (int r = 0; r < RPW; ++r)
-                if (vcur[r])
-                    buf[j][r] = __ldg(reinterpret_cast<const uint4 *>(gp + r * KC + j * kKStep));
         for (int g = 0; g < ngroups; ++g) {
             bool vnext[RPW];
 #pragma unroll
@@ -277,20 +327,27 @@ cudaError_t launch_cfg(const ArgmaxArgs &a, cudaStream_t s)
         grid = kMaxCtas;
     if (grid < 1)
         grid = 1;
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, (unsigned)grid, kThreads, smem, s, a);
 }
 
 // Per hidden-row count: ring depth and rows per group for each width.
 template <int M, int KM>
 cudaError_t launch_m(const ArgmaxArgs &a, cudaStream_t s)
 {
-    // deeper rings where the registers allow it (no spills at 128 per thread)
-    constexpr int NB = M <= 2 ? 5 : 2;
+    // Ring depth NB (k steps in flight) and rows per group RPW, chosen by
+    // measurement on GB300 among the variants that do not spill at 128
+    // registers: a deep ring for M <= 2; for K = 5,120 and M = 3, 4 two rows
+    // per group with a 5-deep ring beat four rows with a 2-deep one.
     if (a.K == 2560)
-        return launch_cfg<M, KM, 2560, NB, 4>(a, s);
-    if (a.K == 5120)
-        return launch_cfg<M, KM, 5120, NB, 4>(a, s);
+        return launch_cfg<M, KM, 2560, (M <= 2 ? 5 : 2), 4>(a, s);
+    if (a.K == 5120) {
+        if constexpr (M <= 2)
+            return launch_cfg<M, KM, 5120, 5, 4>(a, s);
+        else if constexpr (M <= 4)
+            return launch_cfg<M, KM, 5120, 5, 2>(a, s);
+        else
+            return launch_cfg<M, KM, 5120, 2, 4>(a, s);
+    }
     return launch_cfg<M, KM, 0, 2, 4>(a, s);
 }
 

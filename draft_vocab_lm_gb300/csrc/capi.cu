@@ -109,7 +109,7 @@ dvl_status check_head(const dvl_head *hd)
         return DVL_ERR_INVALID_ARG;
     if (hd->dtype != DVL_BF16 && hd->dtype != DVL_NVFP4)
         return DVL_ERR_INVALID_ARG;
-    if (hd->reserved != 0 || hd->reserved2 != 0)
+    if ((hd->flags & ~DVL_HEAD_STATIC) != 0 || hd->reserved2 != 0)
         return DVL_ERR_INVALID_ARG;
     if (hd->N < 1 || hd->K < DVL_K_MULTIPLE || hd->K % DVL_K_MULTIPLE != 0 || hd->K > DVL_MAX_K)
         return DVL_ERR_INVALID_ARG;
@@ -151,6 +151,7 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
     a.gscale = hd->global_scale;
     a.d2t = hd->d2t;
     a.id_base = hd->id_base;
+    a.head_static = (hd->flags & DVL_HEAD_STATIC) != 0;
     a.N = hd->N;
     a.K = hd->K;
     a.k = k;

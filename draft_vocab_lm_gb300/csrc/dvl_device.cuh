@@ -21,6 +21,15 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p)
     return v;
 }
 
+// Programmatic dependent launch: allow the next kernel on the stream to
+// start launching; wait until the preceding kernel has completed and its
+// memory operations are visible.  Both are no-ops without a dependency.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // The two bfloat16 halves of a 32-bit word as fp32 (exact: a bf16 is the
 // upper half of a binary32).  The lower half is the element at the lower
 // address.

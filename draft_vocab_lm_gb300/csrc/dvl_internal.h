@@ -31,6 +31,7 @@ struct ArgmaxArgs {
     float *logits;            // [M][k] of this chunk
     int k;                    // results per row (1 .. kmax)
     unsigned char *ws;        // workspace base
+    bool head_static;         // w / scales / d2t not written by pending work
 };
 
 // Per-device facts, queried once.
@@ -60,5 +61,26 @@ dvl_status check_reduce_args(const dvl_head *hd, const void *h, int32_t M, int32
 cudaError_t launch_trim_rows(const unsigned char *src, int64_t src_row_bytes,
                              unsigned char *dst, const int32_t *ranks, int n,
                              cudaStream_t s);
+
+// Launch `kern` on `s` with programmatic stream serialization allowed, so it
+// may begin while the preceding kernel on the stream finishes (the kernel
+// itself waits, with griddepcontrol.wait, before it reads that kernel's
+// results).
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                       const Args &...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 }  // namespace dvl

@@ -70,12 +70,21 @@ typedef enum {
 #define DVL_K_MULTIPLE 64   /* K must be a positive multiple of this           */
 #define DVL_MAX_K 24576     /* largest hidden width                            */
 
+/* dvl_head.flags: the caller promises that no work still pending on the
+ * stream when the call is enqueued writes w, scales or d2t (true of weights
+ * loaded long before; not of a head trim_head has just filled on the same
+ * stream unless the caller synchronized since).  The kernel may then start
+ * streaming the head before the preceding kernel on the stream has finished
+ * (programmatic dependent launch); without the flag it reads nothing before
+ * that kernel completes. */
+#define DVL_HEAD_STATIC 1
+
 /* A draft head as the kernels read it.  Every pointer is device memory. */
 typedef struct dvl_head {
     int32_t dtype;        /* dvl_dtype                                         */
     int32_t N;            /* rows of W (>= 1)                                  */
     int32_t K;            /* hidden width (multiple of 64, <= DVL_MAX_K)       */
-    int32_t reserved;     /* must be 0                                         */
+    int32_t flags;        /* DVL_HEAD_* bits; 0 when none applies              */
     int64_t V;            /* full vocabulary size: ids lie in [0, V)           */
     int64_t id_base;      /* with d2t == NULL, row n has full id id_base + n;
                              id_base + N <= V.  0 for a whole head; the first
@@ -137,7 +146,7 @@ dvl_status dvl_workspace_init(void *ws, size_t bytes, void *stream);
  *   ws:        device workspace of at least dvl_workspace_bytes(M, 1)
  *              bytes, zeroed once by dvl_workspace_init.
  * Errors: DVL_ERR_INVALID_ARG (NULL, misaligned, N < 1, K not a multiple of
- * 64 or above DVL_MAX_K, M out of range, reserved fields non-zero, dtype
+ * 64 or above DVL_MAX_K, M out of range, unknown flags, reserved2 non-zero, dtype
  * unknown, NVFP4 without scales, d2t == NULL with id_base + N > V),
  * DVL_ERR_WORKSPACE, DVL_ERR_CUDA. */
 dvl_status dvl_draft_argmax(const dvl_head *head, const void *h, int32_t M,

@@ -215,3 +215,46 @@ def test_trim_head_small_with_duplicates(dvl, oracle_mod):
     q_t, s_t, d2t2, _ = dvl.trim_head(dev(q), ranks, scales=dev(sc))
     assert oracle_mod.check_trim(q, ranks, q_t.cpu().numpy(), d2t2.cpu().numpy()) == 0
     assert oracle_mod.check_trim(sc, ranks, s_t.cpu().numpy(), None) == 0
+
+
+@pytest.mark.parametrize("static", [False, True])
+def test_back_to_back_calls_with_overlapping_launches(dvl, oracle_mod, static):
+    # consecutive calls may overlap (programmatic dependent launch); each must
+    # still see its own hidden rows and a clean workspace, and a static head
+    # may be streamed before the previous call ends
+    rng = np.random.default_rng(21 + static)
+    N, K = 16000, 2560
+    w = int_bf16(rng, (N, K))
+    head = dvl.Head(dev(w), static=static)
+    ws = dvl.make_workspace(4, 4)
+    hs = [int_bf16(rng, (M, K)) for M in (1, 3, 2, 1, 3, 4)]
+    outs = []
+    for h in hs:
+        ids = torch.empty(h.shape[0], dtype=torch.int32, device="cuda")
+        vals = torch.empty(h.shape[0], dtype=torch.float32, device="cuda")
+        dvl.draft_argmax(head, dev(h), ids=ids, logits=vals, ws=ws)
+        outs.append((ids, vals))
+    for h, (ids, vals) in zip(hs, outs):
+        L, _ = oracle_mod.logits_bf16(w, h)
+        o_ids, o_vals = oracle_mod.argmax(L)
+        assert np.array_equal(ids.cpu().numpy(), o_ids)
+        assert np.array_equal(vals.cpu().numpy(), o_vals)
+
+
+def test_trim_then_argmax_without_synchronizing(dvl, oracle_mod):
+    # the argmax right after trim_head on the same stream must read the
+    # trimmed rows, not what the buffer held before
+    V, K = 6000, 2560
+    rng = np.random.default_rng(33)
+    wfull = int_bf16(rng, (V, K))
+    wfull_d = dev(wfull)
+    h = int_bf16(rng, (2, K))
+    hd = dev(h)
+    for it in range(3):
+        ranks = rng.permutation(V)[:2500].astype(np.int32)
+        w_trim, _, d2t, _ = dvl.trim_head(wfull_d, ranks)
+        ids, vals = dvl.draft_argmax(dvl.Head(w_trim, V=V, d2t=d2t), hd)
+        L, _ = oracle_mod.logits_bf16(wfull[ranks], h)
+        o_ids, o_vals = oracle_mod.argmax(L, ranks)
+        assert np.array_equal(ids.cpu().numpy(), o_ids), it
+        assert np.array_equal(vals.cpu().numpy(), o_vals), it

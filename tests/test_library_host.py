@@ -110,7 +110,7 @@ def _head(**kw):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(dtype=7), dict(N=0), dict(K=100), dict(K=0), dict(K=24576 + 64), dict(reserved=1),
+    dict(dtype=7), dict(N=0), dict(K=100), dict(K=0), dict(K=24576 + 64), dict(flags=2), dict(reserved2=1),
     dict(w=None), dict(w=0x1004), dict(dtype=1), dict(V=50), dict(id_base=1),
 ])
 def test_argument_checks_reject_before_any_launch(dvl, bad):
