@@ -52,6 +52,9 @@ cudaError_t blocks_per_sm(const void *func, int threads, size_t smem, int *out);
 cudaError_t launch_argmax_bf16(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
 cudaError_t launch_argmax_nvfp4(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
 int max_chunk_rows_bf16(int K);
+// Tensor-core argmax (bf16, k = 1) for 9..32 hidden rows in one launch.
+bool tc_argmax_supported(int M, int K);
+cudaError_t launch_argmax_tc(const ArgmaxArgs &a, int M, cudaStream_t s);
 int max_chunk_rows_nvfp4(int K);
 
 // The argument checks of draft_argmax / draft_topk, without the workspace.
