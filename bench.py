@@ -48,8 +48,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--quick", action="store_true", help="headline only")
     p.add_argument("--repeats", type=int, default=5)
-    p.add_argument("--profile", action="store_true",
-                   help="only warm-up + timed headline calls (for ncu captures)")
+    p.add_argument("--profile", nargs="?", const="c2m1", default=None,
+                   help="only warm-up + timed calls of one workload, for ncu captures: "
+                        "c2m1 (default), c2m3, c1m1, c1m3, c3m1, c4m8, c4m16, c4m32, c5m1, c5m3")
     return p.parse_args()
 
 
@@ -259,6 +260,50 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------
 
+def run_profile(args):
+    """Warm-up plus `steps` calls of one workload and nothing else: the
+    command ncu captures.  Inputs are the workloads' own (seeded)."""
+    import torch
+    import draft_vocab_lm_gb300 as dvl
+    from draft_vocab_lm_gb300 import build as B
+    B.build()
+    name = args.profile
+    cfg, M = name[:2], int(name.split("m")[1])
+    ws = dvl.make_workspace(32, 1)
+    if cfg == "c2":
+        wl = S.c2(Ms=(M,))
+        head = dvl.Head(dev(torch, wl.w), V=wl.V, static=True)
+    elif cfg == "c1":
+        wl = S.c1(with_full=False)
+        head = dvl.Head(dev(torch, wl.w), V=wl.V, d2t=dev(torch, wl.d2t), static=True)
+        wl.h = {M: S.hidden_bf16(M, M, wl.K)}
+    elif cfg == "c3":
+        wl = S.c3(Ms=(M,), S=1_000_000)
+        counts = dvl.histogram(wl.extra["tokens"], wl.V)
+        ranks = dvl.build_ranks(counts, wl.extra["N"])
+        w_trim, _, d2t, _ = dvl.trim_head(dev(torch, wl.w_full), ranks)
+        torch.cuda.synchronize()
+        head = dvl.Head(w_trim, V=wl.V, d2t=d2t, static=True)
+    elif cfg == "c4":
+        wl = S.c4(Ms=(M,))
+        head = dvl.Head(dev(torch, wl.extra["w_by_M"][M]), V=wl.V, d2t=dev(torch, wl.d2t),
+                        static=True)
+    elif cfg == "c5":
+        wl = S.c5(Ms=(M,))
+        head = dvl.Head(dev(torch, wl.q), scales=dev(torch, wl.scales), global_scale=wl.g,
+                        V=wl.V, d2t=dev(torch, wl.d2t), static=True)
+    else:
+        raise SystemExit(f"unknown profile workload {name}")
+    h = dev(torch, wl.h[M])
+    ids = torch.empty(M, dtype=torch.int32, device="cuda")
+    lg = torch.empty(M, dtype=torch.float32, device="cuda")
+    n = max(3, args.warmup) + args.steps
+    for _ in range(n):
+        dvl.draft_argmax(head, h, ids=ids, logits=lg, ws=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": name, "launches": n}))
+
+
 def run_ours(args):
     import torch
     import draft_vocab_lm_gb300 as dvl
@@ -300,12 +345,6 @@ def run_ours(args):
     for i in range(max(3, args.warmup)):
         call_m1(i)
     torch.cuda.synchronize()
-    if args.profile:
-        for i in range(args.steps):
-            call_m1(i)
-        torch.cuda.synchronize()
-        print(json.dumps({"profile_run": "ok", "launches": max(3, args.warmup) + args.steps}))
-        return
     sampler = ClockSampler(gpu_id)
     time.sleep(0.3)
     if dist:
@@ -530,6 +569,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.profile:
+        run_profile(args)
     else:
         run_ours(args)
 

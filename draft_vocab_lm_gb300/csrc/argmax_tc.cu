@@ -1,5 +1,5 @@
 // Fused skinny projection + argmax on the tensor cores (tcgen05, TMEM) for
-// batched drafting: 9 to 32 hidden rows at once ("[DGX Spark]
+// batched drafting: 5 to 32 hidden rows at once ("[DGX Spark]
 // Qwen3.8-Flash-Next on two DGX Sparks", section "Five changes in 16 days":
 // MTP with 4 draft slots, 8 concurrent streams; "Shortlist MTP", section
 // "At first, the shortlist looked REALLY good": 8 concurrent requests).  With
@@ -11,9 +11,10 @@
 // rows (A = W tile, K-major; B = h, K-major; NM = 16 or 32 >= M), fp32 in
 // tensor memory.  One block of 8 warps per SM, each on a contiguous range of
 // rows split into 128-row tiles:
-//   warp 0   TMA producer: per 64-wide k step, the W tile [128 x 64] and the
-//            h tile [NM x 64] (128-byte swizzle) into a ring of S stages;
-//   warp 1   MMA issuer: 4 tcgen05.mma (K = 16 each) per stage into one of
+//   warp 0   TMA producer: per stage, two 64-wide k steps of the W tile
+//            [128 x 64] and the h tile [NM x 64] (128-byte swizzle) into a
+//            ring of S stages;
+//   warp 1   MMA issuer: 8 tcgen05.mma (K = 16 each) per stage into one of
 //            two TMEM accumulators; commits free the stage, and a finished
 //            tile's accumulator;
 //   warp 2   allocates and frees the TMEM columns;
@@ -46,14 +47,18 @@ constexpr int kBK = 64;                // k per stage (one 128-byte swizzle row)
 constexpr int kWTile = kBM * kBK * 2;  // 16 KB
 constexpr int kEpiWarp0 = 4;           // warps 4..7: TMEM lane quadrants 0..3
 
+constexpr int kBoxes = 2;              // 64-wide k boxes per pipeline stage
+
 template <int NM>
 struct TcLayout {
     static constexpr int kHTile = NM * kBK * 2;
-    static constexpr int kStages = NM == 32 ? 8 : 9;
+    static constexpr int kWStage = kBoxes * kWTile;
+    static constexpr int kHStage = kBoxes * kHTile;
+    static constexpr int kStages = (NM == 32 ? 8 : 9) / kBoxes;
     static constexpr int kTmemCols = 2 * NM < 32 ? 32 : 2 * NM;
     static constexpr size_t w_off = 0;
-    static constexpr size_t h_off = w_off + (size_t)kStages * kWTile;
-    static constexpr size_t bar_off = h_off + (size_t)kStages * kHTile;
+    static constexpr size_t h_off = w_off + (size_t)kStages * kWStage;
+    static constexpr size_t bar_off = h_off + (size_t)kStages * kHStage;
     // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
     static constexpr size_t misc_off = bar_off + (size_t)(2 * kStages + 5) * 8;
     // tmem base, abort flag, issued, consumed
@@ -152,15 +157,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < ntiles; ++t) {
                 const int row = r0 + t * kBM;
                 bool ok = true;
-                for (int kc = 0; kc < KC; ++kc, ++i) {
+                for (int kc = 0; kc < KC; kc += kBoxes, ++i) {
                     const int s = (int)(i % S);
                     if (!wait_or_abort(&empty[s], ((i / S) & 1u) ^ 1u, abort_flag, a.ws)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(kWTile + L::kHTile));
-                    tc::tma_load_2d(sW + (size_t)s * kWTile, &tmap_w, kc * kBK, row, &full[s]);
-                    tc::tma_load_2d(sH + (size_t)s * L::kHTile, &tmap_h, kc * kBK, 0, &full[s]);
+                    const int nb = min(kBoxes, KC - kc);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nb * (kWTile + L::kHTile)));
+                    for (int bx = 0; bx < nb; ++bx) {
+                        tc::tma_load_2d(sW + (size_t)s * L::kWStage + bx * kWTile, &tmap_w,
+                                        (kc + bx) * kBK, row, &full[s]);
+                        tc::tma_load_2d(sH + (size_t)s * L::kHStage + bx * L::kHTile, &tmap_h,
+                                        (kc + bx) * kBK, 0, &full[s]);
+                    }
                     misc[2] = i + 1;
                 }
                 if (!ok)
@@ -178,20 +188,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_after_thread_sync();
                 const uint32_t d = tmem_base + (uint32_t)(b * NM);
                 bool ok = true;
-                for (int kc = 0; kc < KC; ++kc, ++i) {
+                for (int kc = 0; kc < KC; kc += kBoxes, ++i) {
                     const int s = (int)(i % S);
                     if (!wait_or_abort(&full[s], (i / S) & 1u, abort_flag, a.ws)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_thread_sync();
-                    const unsigned char *wt = sW + (size_t)s * kWTile;
-                    const unsigned char *ht = sH + (size_t)s * L::kHTile;
+                    const int nb = min(kBoxes, KC - kc);
+                    for (int bx = 0; bx < nb; ++bx) {
+                        const unsigned char *wt = sW + (size_t)s * L::kWStage + bx * kWTile;
+                        const unsigned char *ht = sH + (size_t)s * L::kHStage + bx * L::kHTile;
 #pragma unroll
-                    for (int k16 = 0; k16 < kBK / 16; ++k16)
-                        tc::mma_bf16(d, tc::sw128_kmajor_desc(wt + 32 * k16),
-                                     tc::sw128_kmajor_desc(ht + 32 * k16), idesc,
-                                     (kc | k16) != 0);
+                        for (int k16 = 0; k16 < kBK / 16; ++k16)
+                            tc::mma_bf16(d, tc::sw128_kmajor_desc(wt + 32 * k16),
+                                         tc::sw128_kmajor_desc(ht + 32 * k16), idesc,
+                                         (kc + bx) > 0 || k16 > 0);
+                    }
                     tc::mma_commit(&empty[s]);  // the stage is free once these MMAs finish
                     misc[3] = i + 1;
                 }
@@ -331,7 +344,7 @@ cudaError_t launch_nm(const ArgmaxArgs &a, int M, cudaStream_t s)
 
 }  // namespace
 
-bool tc_argmax_supported(int M, int K) { return M > 8 && M <= 32 && K % kBK == 0; }
+bool tc_argmax_supported(int M, int K) { return M > 4 && M <= 32 && K % kBK == 0; }
 
 cudaError_t launch_argmax_tc(const ArgmaxArgs &a, int M, cudaStream_t s)
 {
