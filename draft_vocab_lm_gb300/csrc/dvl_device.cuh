@@ -206,17 +206,15 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
     if (!s_last)
         return;
     __threadfence();
-    if (KM == 1) {
+    if constexpr (KM == 1) {
         // one thread per hidden row: the swaps go out together
         for (int m = threadIdx.x; m < M; m += blockDim.x) {
             uint64_t key = atomicExch(best + m, 0ull);
             a.ids[m] = key_id(key);
             a.logits[m] = key_logit(key);
         }
-        return;
-    }
-    for (int m = warp; m < M; m += nwarps) {
-        {
+    } else {
+        for (int m = warp; m < M; m += nwarps) {
             TopList<KM> L;
             L.init();
             for (int c = lane; c < (int)gridDim.x; c += 32)
