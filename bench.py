@@ -36,7 +36,8 @@ import synthetic as S  # noqa: E402
 from draft_vocab_lm_gb300 import roofline as RL  # noqa: E402
 
 METRIC = "draft_argmax calls/s and achieved HBM GB/s (% of peak) at M=1,3; trim vs full"
-HEADLINE_KERNEL_SOURCES = ("draft_vocab_lm_gb300/csrc/argmax_bf16.cu",
+HEADLINE_KERNEL_SOURCES = ("draft_vocab_lm_gb300/csrc/argmax_bf16.cuh",
+                           "draft_vocab_lm_gb300/csrc/argmax_bf16_m12.cu",
                            "draft_vocab_lm_gb300/csrc/dvl_device.cuh")
 
 

@@ -1,354 +1,19 @@
-// Fused projection + argmax / top-k over an NVFP4 draft head.  ("Masked MTP
-// drafts": requantizing the trimmed head to NVFP4 costs no measured
-// acceptance; the head read shrinks a further 3.6x against bf16.)
-//
-// Format read here: codes [N][K/2], two E2M1 values per byte with the even k
-// in the low nibble; scales [N][K/16], one E4M3 per 16 consecutive k of a
-// row; one fp32 tensor scale g.  weight = e2m1 * e4m3 * g.
-//
-// Decoding on CUDA cores costs more instructions per weight than HBM leaves
-// time for, so the products run on the tensor cores through the register
-// path (mma.sync m16n8k16, f16 inputs, fp32 accumulation), which takes its
-// A operand straight from the registers the codes were decoded into:
-//   - a warp owns 16 head rows; lane (g, q) reads 16 bytes of codes (32
-//     weights, two scale blocks) of rows g and g + 8 per 128-wide k chunk, so
-//     a quad reads 64 contiguous bytes of each row;
-//   - each code byte becomes an f16 pair with the exact E2M1x2 -> f16x2
-//     conversion and is multiplied by its block's E4M3 scale (E4M3x2 ->
-//     f16x2); the product has at most 6 significant bits and lies in
-//     [2^-10, 2688], so it is exact in f16;
-//   - the hidden rows are staged once per block as f16 after an exact
-//     power-of-two rescale that puts their largest magnitude in [2^14, 2^15)
-//     (bf16 values within 2^31 of that maximum convert exactly; smaller ones
-//     round at 2^-24 of the rescaled range); the rescale and g are applied to
-//     the finished fp32 dot;
-//   - the k order inside an MMA is a permutation of the weights' k, the same
-//     for A and B, so every product pairs the right weight and hidden value.
-// Results go through the same per-lane lists, block merge and cross-block
-// finish as the bf16 kernels.
-#include <cuda_fp16.h>
-#include <cuda_runtime.h>
-
-#include "dvl_device.cuh"
+// Dispatch of the NVFP4 argmax / top-k kernel (argmax_nvfp4.cuh) to its
+// instantiations.
+#include "argmax_nvfp4.cuh"
 
 namespace dvl {
-namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kRows = 16;      // head rows per warp group (MMA M)
-constexpr int kChunk = 128;    // weights per row per k chunk (64 bytes of codes)
-constexpr int kNB = 4;         // k chunks of loads in flight per lane
-constexpr int kLists = kWarps * 8;  // candidate lists per hidden row (8 row pairs per warp)
-
-// Four bytes of codes -> four f16x2 (byte t: low nibble in the low half).
-__device__ __forceinline__ void e2m1_word(uint32_t w, uint32_t (&f)[4])
-{
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
-        : "r"(w));
-}
-
-// Two E4M3 scales (low byte first) -> f16x2, and each broadcast to a pair.
-__device__ __forceinline__ void e4m3_pair(uint32_t s16, uint32_t &lo2, uint32_t &hi2)
-{
-    uint32_t p;
-    const uint16_t s = (uint16_t)s16;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(p) : "h"(s));
-    lo2 = __byte_perm(p, p, 0x1010);
-    hi2 = __byte_perm(p, p, 0x3232);
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ float pow2f(int e)  // 2^e for e in [-126, 127], exact
-{
-    return __int_as_float((127 + e) << 23);
-}
-
-// Shared memory: the rescaled hidden rows as f16, in 16-byte units ordered
-// [chunk][u][g][q] with g < M (unit = h[g][128 chunk + 32 q + 8 u .. +8]), so
-// that the reading lanes' units for one u are contiguous.  Lanes whose MMA
-// column g is M or more feed zeros and read nothing.
-__host__ __device__ inline size_t nvfp4_h_bytes(int Kpad, int M) { return (size_t)Kpad * 2 * M; }
-
-template <int M, int KM>
-__global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxArgs a)
-{
-    extern __shared__ __align__(16) unsigned char smem[];
-    const int K = a.K, Kpad = a.Kpad, C = Kpad / kChunk;
-    uint4 *s_h = reinterpret_cast<uint4 *>(smem);
-    uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + nvfp4_h_bytes(Kpad, M));
-    __shared__ int s_shift;
-    __shared__ unsigned int s_hmax;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, q = lane & 3;
-    const uint8_t *__restrict__ Q = static_cast<const uint8_t *>(a.w);
-    const uint8_t *__restrict__ S = a.scales;
-    const size_t qrow = (size_t)K / 2, srow = (size_t)K / 16;
-
-    pdl_launch_dependents();
-    pdl_wait();
-
-    // Largest |h| (bf16 magnitudes order like their bit patterns).
-    if (tid == 0)
-        s_hmax = 0u;
-    __syncthreads();
-    {
-        unsigned int mx = 0u;
-        for (int i = tid; i < M * K / 2; i += kThreads) {
-            const uint32_t x = __ldg(reinterpret_cast<const uint32_t *>(a.h) + i);
-            mx = max(mx, max(x & 0x7fffu, (x >> 16) & 0x7fffu));
-        }
-        for (int off = 16; off >= 1; off >>= 1)
-            mx = max(mx, __shfl_xor_sync(kFull, mx, off));
-        if (lane == 0)
-            atomicMax(&s_hmax, mx);
-    }
-    for (int i = tid; i < M * kLists * KM; i += kThreads)
-        s_cand[i] = 0ull;
-    __syncthreads();
-    if (tid == 0) {
-        // shift so that max|h| * 2^shift lies in [2^14, 2^15)
-        // hmax = f * 2^e with f in [0.5, 1): e = biased exponent - 126
-        const int ef = (int)(s_hmax >> 7);  // exponent field of the bf16
-        const int sh = s_hmax == 0u ? 0 : (ef == 0 ? 100 : 15 - (ef - 126));
-        s_shift = min(max(sh, -100), 100);
-    }
-    __syncthreads();
-    const int shift = s_shift;
-    {
-        const float up = shift >= 0 ? pow2f(min(shift, 127)) : pow2f(max(shift, -126));
-        const int nunits = C * 4 * M * 4;
-        for (int i = tid; i < nunits; i += kThreads) {
-            const int qq = i & 3, r = i >> 2;
-            const int gg = r % M, u = (r / M) & 3, c = r / (M * 4);
-            const int k0 = kChunk * c + 32 * qq + 8 * u;
-            uint32_t hv[4] = {0u, 0u, 0u, 0u};
-            if (k0 < K) {
-                const uint4 x = __ldg(reinterpret_cast<const uint4 *>(a.h + (size_t)gg * K + k0));
-                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const __half2 hh = __floats2half2_rn(bf16_lo(xs[j]) * up, bf16_hi(xs[j]) * up);
-                    hv[j] = *reinterpret_cast<const uint32_t *>(&hh);
-                }
-            }
-            s_h[i] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        }
-    }
-    __syncthreads();
-    const float down = (shift >= 0 ? pow2f(max(-shift, -126)) : pow2f(min(-shift, 127))) * a.gscale;
-
-    // Warps take 16-row groups round robin over the whole grid.
-    const int ngroups = (a.N + kRows - 1) / kRows;
-    const int GW = gridDim.x * kWarps;
-    const int gw = blockIdx.x * kWarps + warp;
-    const int my_groups = gw < ngroups ? (ngroups - 1 - gw) / GW + 1 : 0;
-    const int total = my_groups * C;
-
-    TopList<KM> best0, best1;  // hidden rows 2q and 2q + 1
-    best0.init();
-    best1.init();
-    // four independent accumulators, so consecutive MMAs do not wait on
-    // each other; summed at the end of a group
-    float acc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-
-    uint4 bqa[kNB], bqb[kNB];
-    uint32_t bsa[kNB], bsb[kNB];
-    int li = 0, lc = 0;  // load cursor (my group index, chunk)
-    auto issue = [&](int b) {
-        const int grp = gw + li * GW;
-        const int ra = grp * kRows + g, rb = ra + 8;
-        const int kc = kChunk * lc + 32 * q;
-        const bool kin = li < my_groups && kc < K;
-        bqa[b] = make_uint4(0u, 0u, 0u, 0u);
-        bqb[b] = make_uint4(0u, 0u, 0u, 0u);
-        bsa[b] = 0u;
-        bsb[b] = 0u;
-        if (kin && ra < a.N) {
-            bqa[b] = ld_stream16(Q + (size_t)ra * qrow + kc / 2);
-            bsa[b] = __ldg(reinterpret_cast<const unsigned short *>(S + (size_t)ra * srow + kc / 16));
-        }
-        if (kin && rb < a.N) {
-            bqb[b] = ld_stream16(Q + (size_t)rb * qrow + kc / 2);
-            bsb[b] = __ldg(reinterpret_cast<const unsigned short *>(S + (size_t)rb * srow + kc / 16));
-        }
-        if (++lc == C) {
-            lc = 0;
-            ++li;
-        }
-    };
-    int ci = 0, cc = 0;  // consume cursor
-    int ida = 0, idb = 0;
-    auto consume = [&](int b) {
-        const int grp = gw + ci * GW;
-        const int ra = grp * kRows + g, rb = ra + 8;
-        if (cc == 0) {
-            ida = ra < a.N ? (a.d2t ? __ldg(a.d2t + ra) : (int)(a.id_base + ra)) : 0;
-            idb = rb < a.N ? (a.d2t ? __ldg(a.d2t + rb) : (int)(a.id_base + rb)) : 0;
-        }
-        uint32_t hw[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            hw[j] = 0u;
-        if (g < M) {
-            const uint4 *hp = s_h + (size_t)cc * (16 * M) + (g * 4 + q);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint4 v = hp[u * 4 * M];
-                hw[4 * u] = v.x; hw[4 * u + 1] = v.y; hw[4 * u + 2] = v.z; hw[4 * u + 3] = v.w;
-            }
-        }
-        uint32_t sa_lo, sa_hi, sb_lo, sb_hi;
-        e4m3_pair(bsa[b], sa_lo, sa_hi);
-        e4m3_pair(bsb[b], sb_lo, sb_hi);
-        uint32_t fa[16], fb[16];
-        const uint32_t wa[4] = {bqa[b].x, bqa[b].y, bqa[b].z, bqa[b].w};
-        const uint32_t wb[4] = {bqb[b].x, bqb[b].y, bqb[b].z, bqb[b].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t t4[4];
-            e2m1_word(wa[j], t4);
-            fa[4 * j] = t4[0]; fa[4 * j + 1] = t4[1]; fa[4 * j + 2] = t4[2]; fa[4 * j + 3] = t4[3];
-            e2m1_word(wb[j], t4);
-            fb[4 * j] = t4[0]; fb[4 * j + 1] = t4[1]; fb[4 * j + 2] = t4[2]; fb[4 * j + 3] = t4[3];
-        }
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const uint32_t sca = t < 4 ? sa_lo : sa_hi, scb = t < 4 ? sb_lo : sb_hi;
-            mma_f16(acc[t & 3], hmul2(fa[2 * t], sca), hmul2(fb[2 * t], scb), hmul2(fa[2 * t + 1], sca),
-                    hmul2(fb[2 * t + 1], scb), hw[2 * t], hw[2 * t + 1]);
-        }
-        if (++cc == C) {
-            // rows ra (c0, c1) and rb (c2, c3); hidden rows 2q and 2q + 1
-            float d[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                d[j] = (acc[0][j] + acc[1][j]) + (acc[2][j] + acc[3][j]);
-                acc[0][j] = acc[1][j] = acc[2][j] = acc[3][j] = 0.f;
-            }
-            if (ra < a.N) {
-                if (2 * q < M)
-                    best0.insert(make_key(d[0] * down, ida));
-                if (2 * q + 1 < M)
-                    best1.insert(make_key(d[1] * down, ida));
-            }
-            if (rb < a.N) {
-                if (2 * q < M)
-                    best0.insert(make_key(d[2] * down, idb));
-                if (2 * q + 1 < M)
-                    best1.insert(make_key(d[3] * down, idb));
-            }
-            cc = 0;
-            ++ci;
-        }
-    };
-
-#pragma unroll
-    for (int b = 0; b < kNB; ++b)
-        issue(b);
-    for (int t0 = 0; t0 < total; t0 += kNB) {
-#pragma unroll
-        for (int b = 0; b < kNB; ++b) {
-            if (t0 + b < total)
-                consume(b);
-            issue(b);
-        }
-    }
-
-    const int slot = warp * 8 + g;
-    if (2 * q < M) {
-#pragma unroll
-        for (int i = 0; i < KM; ++i)
-            s_cand[((2 * q) * kLists + slot) * KM + i] = best0.v[i];
-    }
-    if (2 * q + 1 < M) {
-#pragma unroll
-        for (int i = 0; i < KM; ++i)
-            s_cand[((2 * q + 1) * kLists + slot) * KM + i] = best1.v[i];
-    }
-    __syncthreads();
-    block_finish<KM>(s_cand, M, kLists, a);
-}
-
-template <int M, int KM>
-cudaError_t launch_one(const ArgmaxArgs &a, cudaStream_t s)
-{
-    const size_t smem = nvfp4_h_bytes(a.Kpad, M) + (size_t)M * kLists * KM * 8;
-    DeviceInfo di;
-    cudaError_t e = device_info(&di);
-    if (e != cudaSuccess)
-        return e;
-    auto kern = argmax_nvfp4_kernel<M, KM>;
-    int per_sm = 0;
-    e = blocks_per_sm(reinterpret_cast<const void *>(kern), kThreads, smem, &per_sm);
-    if (e != cudaSuccess)
-        return e;
-    if (per_sm < 1)
-        return cudaErrorInvalidConfiguration;
-    if (per_sm > 2)
-        per_sm = 2;
-    const long long groups = ((long long)a.N + kRows - 1) / kRows;
-    long long grid = (long long)di.sms * per_sm;
-    const long long max_by_groups = (groups + kWarps - 1) / kWarps;  // >= 1 group per warp
-    if (grid > max_by_groups)
-        grid = max_by_groups;
-    if (grid > kMaxCtas)
-        grid = kMaxCtas;
-    if (grid < 1)
-        grid = 1;
-    return launch_pdl(kern, (unsigned)grid, kThreads, smem, s, a);
-}
-
-template <int KM>
-cudaError_t dispatch_m(const ArgmaxArgs &a, int M, cudaStream_t s)
-{
-    switch (M) {
-    case 1: return launch_one<1, KM>(a, s);
-    case 2: return launch_one<2, KM>(a, s);
-    case 3: return launch_one<3, KM>(a, s);
-    case 4: return launch_one<4, KM>(a, s);
-    case 5: return launch_one<5, KM>(a, s);
-    case 6: return launch_one<6, KM>(a, s);
-    case 7: return launch_one<7, KM>(a, s);
-    case 8: return launch_one<8, KM>(a, s);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
-}  // namespace
+cudaError_t launch_argmax_nvfp4_kc(const ArgmaxArgs &a, int M, cudaStream_t s);
+cudaError_t launch_argmax_nvfp4_rt(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
 
 // Hidden rows per launch: up to 8 (one MMA n8 tile), and few enough that the
 // staged hidden rows leave room for two blocks per SM; 0 if not even one fits.
 int max_chunk_rows_nvfp4(int K)
 {
-    const int Kpad = (K + kChunk - 1) / kChunk * kChunk;
+    const int Kpad = nvfp4::kpad_of(K);
     for (int M = 8; M >= 1; --M)
-        if (nvfp4_h_bytes(Kpad, M) + (size_t)M * kLists * 4 * 8 <= 110 * 1024)
+        if (nvfp4::nvfp4_h_bytes(Kpad, M) + (size_t)M * nvfp4::kLists * 4 * 8 <= 110 * 1024)
             return M;
     return 0;
 }
@@ -356,8 +21,12 @@ int max_chunk_rows_nvfp4(int K)
 cudaError_t launch_argmax_nvfp4(const ArgmaxArgs &a_in, int M, int kmax, cudaStream_t s)
 {
     ArgmaxArgs a = a_in;
-    a.Kpad = (a.K + kChunk - 1) / kChunk * kChunk;
-    return kmax == 1 ? dispatch_m<1>(a, M, s) : dispatch_m<4>(a, M, s);
+    a.Kpad = nvfp4::kpad_of(a.K);
+    // argmax at the unrolled widths: one base pointer per group with
+    // immediate offsets (measured 29.0 -> 20.4 us on a 32k x 5,120 head)
+    if (kmax == 1 && M <= 4 && (a.K == 5120 || a.K == 2560))
+        return launch_argmax_nvfp4_kc(a, M, s);
+    return launch_argmax_nvfp4_rt(a, M, kmax, s);
 }
 
 }  // namespace dvl

@@ -158,7 +158,7 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
     a.ws = static_cast<unsigned char *>(ws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (hd->dtype == DVL_BF16 && k == 1 && tc_argmax_supported(M, hd->K)) {
-        // 9..32 rows: one pass on the tensor cores instead of several
+        // 5..32 rows: one pass on the tensor cores instead of several
         // CUDA-core passes over the head
         a.h = static_cast<const uint16_t *>(h);
         a.ids = ids;
