@@ -103,23 +103,35 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t x)
     return x;
 }
 
-// Take the warp's `k` best keys out of the lanes' lists, best first; every
-// lane receives them.  Equal keys are taken one at a time (lowest lane first).
+// Butterfly merge of the lanes' lists: afterwards every lane's list holds
+// the warp's KM best keys (KM a power of two), best first.  At each level a
+// lane swaps lists with its partner; the elementwise maximum of one
+// descending list and the other reversed holds the KM largest keys of both
+// as a bitonic sequence, which a bitonic merge network puts in order.
 template <int KM>
-__device__ __forceinline__ void warp_extract(TopList<KM> &L, int k, uint64_t (&out)[KM])
+__device__ __forceinline__ void warp_merge_topk(TopList<KM> &L)
 {
-    const int lane = threadIdx.x & 31;
+    static_assert((KM & (KM - 1)) == 0, "KM must be a power of two");
 #pragma unroll
-    for (int i = 0; i < KM; ++i) {
-        out[i] = 0ull;
-        if (i < k) {
-            uint64_t head = L.v[0];
-            uint64_t best = warp_max_u64(head);
-            unsigned mask = __ballot_sync(kFull, head == best);
-            if (lane == __ffs(mask) - 1)
-                L.pop();
-            out[i] = best;
+    for (int off = 16; off >= 1; off >>= 1) {
+        uint64_t o[KM];
+#pragma unroll
+        for (int i = 0; i < KM; ++i)
+            o[i] = __shfl_xor_sync(kFull, L.v[i], off);
+#pragma unroll
+        for (int i = 0; i < KM; ++i) {
+            const uint64_t b = o[KM - 1 - i];
+            L.v[i] = b > L.v[i] ? b : L.v[i];
         }
+#pragma unroll
+        for (int st = KM / 2; st >= 1; st >>= 1)
+#pragma unroll
+            for (int i = 0; i < KM; ++i)
+                if ((i & st) == 0) {
+                    const uint64_t x = L.v[i], y = L.v[i + st];
+                    L.v[i] = x > y ? x : y;
+                    L.v[i + st] = x > y ? y : x;
+                }
     }
 }
 
@@ -187,13 +199,12 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
             if (lane == 0 && key != 0ull)
                 atomicMax(best + m, (unsigned long long)key);
         } else {
-            uint64_t out[KM];
-            warp_extract<KM>(L, a.k, out);
-            // every lane holds out[]; lane i stores entry i
+            warp_merge_topk<KM>(L);
+            // every lane holds the list; lane i stores entry i
 #pragma unroll
             for (int i = 0; i < KM; ++i)
                 if (lane == i)
-                    slots[((size_t)blockIdx.x * M + m) * KM + i] = out[i];
+                    slots[((size_t)blockIdx.x * M + m) * KM + i] = L.v[i];
         }
     }
     __threadfence();  // this thread's slot stores before the ticket
@@ -214,22 +225,57 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
             a.logits[m] = key_logit(key);
         }
     } else {
-        for (int m = warp; m < M; m += nwarps) {
-            TopList<KM> L;
-            L.init();
-            for (int c = lane; c < (int)gridDim.x; c += 32)
+        // Every warp takes part: warp w merges row w % M over a share of the
+        // blocks, its lanes loading kBatch blocks' slots before inserting any
+        // (one L2 round trip per batch rather than per block); then one warp
+        // per row merges the warps' lists.  The reducing kernels have
+        // M <= nwarps <= kFinWarps whenever k > 1.
+        constexpr int kBatch = 4;
+        constexpr int kFinWarps = 8;
+        __shared__ uint64_t s_fin[kFinWarps][KM];
+        const int wpm = nwarps / M;  // warps per hidden row
+        const int m = warp % M, q = warp / M;
+        TopList<KM> L;
+        L.init();
+        if (q < wpm) {
+            const int stride = 32 * wpm;
+            for (int c0 = 32 * q + lane; c0 < (int)gridDim.x; c0 += kBatch * stride) {
+                uint64_t v[kBatch][KM];
 #pragma unroll
-                for (int i = 0; i < KM; ++i)
-                    L.insert(__ldcg(slots + ((size_t)c * M + m) * KM + i));
-            uint64_t out[KM];
-            warp_extract<KM>(L, a.k, out);
-            if (lane == 0) {
+                for (int u = 0; u < kBatch; ++u) {
+                    const int c = c0 + u * stride;
 #pragma unroll
-                for (int i = 0; i < KM; ++i)
-                    if (i < a.k) {
-                        a.ids[m * a.k + i] = key_id(out[i]);
-                        a.logits[m * a.k + i] = key_logit(out[i]);
-                    }
+                    for (int i = 0; i < KM; ++i)
+                        v[u][i] = c < (int)gridDim.x ? __ldcg(slots + ((size_t)c * M + m) * KM + i)
+                                                     : 0ull;
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+                    for (int i = 0; i < KM; ++i)
+                        L.insert(v[u][i]);
+            }
+        }
+        warp_merge_topk<KM>(L);
+        if (lane == 0 && warp < kFinWarps) {
+#pragma unroll
+            for (int i = 0; i < KM; ++i)
+                s_fin[warp][i] = q < wpm ? L.v[i] : 0ull;
+        }
+        __syncthreads();
+        if (warp < M) {
+            TopList<KM> F;  // the warps' lists are already in order
+#pragma unroll
+            for (int i = 0; i < KM; ++i)
+                F.v[i] = lane < wpm ? s_fin[warp + M * lane][i] : 0ull;
+            warp_merge_topk<KM>(F);
+            if (lane < a.k && lane < KM) {
+                uint64_t key = F.v[0];
+#pragma unroll
+                for (int i = 1; i < KM; ++i)
+                    key = lane == i ? F.v[i] : key;
+                a.ids[warp * a.k + lane] = key_id(key);
+                a.logits[warp * a.k + lane] = key_logit(key);
             }
         }
     }
