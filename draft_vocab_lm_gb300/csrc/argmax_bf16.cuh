@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
     // Stage the hidden rows (bf16 -> fp32, zero past K): 16-byte loads, all
     // of a thread's loads issued before its shared-memory stores.
     {
-        constexpr int kMaxPer = 8;  // covers M * Kpad <= 8 * 8 * 256 elements
+        constexpr int kMaxPer = 10;  // covers M * Kpad <= 10 * 8 * 256 (four rows of 5,120)
         const int nvec = M * (Kpad / 8);
         uint4 v[kMaxPer];
 #pragma unroll

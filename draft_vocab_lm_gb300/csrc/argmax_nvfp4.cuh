@@ -10,9 +10,14 @@
 // time for, so the products run on the tensor cores through the register
 // path (mma.sync m16n8k16, f16 inputs, fp32 accumulation), which takes its
 // A operand straight from the registers the codes were decoded into:
-//   - a warp owns 16 head rows; lane (g, q) reads 16 bytes of codes (32
-//     weights, two scale blocks) of rows g and g + 8 per 128-wide k chunk, so
-//     a quad reads 64 contiguous bytes of each row;
+//   - the grid is persistent (two blocks per SM) and every warp owns one
+//     balanced contiguous range of head rows, walked as 16-row MMA tiles
+//     (the last one partial); lane (g, q) reads 16 bytes of codes (32
+//     weights, two scale blocks) of rows g and g + 8 per 128-wide k chunk,
+//     so a quad reads 64 contiguous bytes of each row;
+//   - a head the caller marked static starts filling the load ring before
+//     the wait for the preceding kernel; for the unrolled widths h is read
+//     from L2 once (its maximum and its staging from the same registers);
 //   - each code byte becomes an f16 pair with the exact E2M1x2 -> f16x2
 //     conversion and is multiplied by its block's E4M3 scale (E4M3x2 ->
 //     f16x2); the product has at most 6 significant bits and lies in
@@ -102,8 +107,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
     const int Kpad = KC > 0 ? KC : a.Kpad, C = Kpad / kChunk;
     uint4 *s_h = reinterpret_cast<uint4 *>(smem);
     uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + nvfp4_h_bytes(Kpad, M));
-    __shared__ int s_shift;
-    __shared__ unsigned int s_hmax;
+    __shared__ unsigned int s_wmax[kWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -112,64 +116,158 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
     const size_t qrow = (size_t)K / 2, srow = (size_t)K / 16;
 
     pdl_launch_dependents();
+
+    // This warp's rows: one balanced contiguous range per warp of the grid,
+    // walked 16 rows (one MMA tile) at a time; the last group may be partial.
+    const long long GW = (long long)gridDim.x * kWarps;
+    const long long gw = (long long)blockIdx.x * kWarps + warp;
+    const int row0 = (int)((long long)a.N * gw / GW);
+    const int rend = (int)((long long)a.N * (gw + 1) / GW);
+    const int my_groups = (rend - row0 + kRows - 1) / kRows;
+
+    // The load ring: codes (16 bytes) and scales (two E4M3) of rows ra / rb.
+    uint4 bqa[kNB], bqb[kNB];
+    uint32_t bsa[kNB], bsb[kNB];
+#pragma unroll
+    for (int b2 = 0; b2 < kNB; ++b2) {
+        bqa[b2] = bqb[b2] = make_uint4(0u, 0u, 0u, 0u);
+        bsa[b2] = bsb[b2] = 0u;
+    }
+    // compile-time K: a group's lane bases, codes of rows ra / rb at byte
+    // 16 q, scales at 2 q; loads are immediate offsets from them
+    constexpr int QR = KC / 2, SR = KC / 16;  // bytes per row: codes, scales
+    auto bases = [&](int li, const uint8_t *&pqa, const uint8_t *&psa, bool &va, bool &vb) {
+        const int ra = row0 + li * kRows + g;
+        va = li < my_groups && ra < rend;
+        vb = li < my_groups && ra + 8 < rend;
+        pqa = Q + (size_t)ra * QR + 16 * q;
+        psa = S + (size_t)ra * SR + 2 * q;
+    };
+    auto load = [&](int b2, const uint8_t *pqa, const uint8_t *psa, bool va, bool vb, int c) {
+        if (va) {
+            bqa[b2] = ld_stream16(pqa + 64 * c);
+            bsa[b2] = __ldg(reinterpret_cast<const unsigned short *>(psa + 8 * c));
+        }
+        if (vb) {
+            bqb[b2] = ld_stream16(pqa + 8 * QR + 64 * c);
+            bsb[b2] = __ldg(reinterpret_cast<const unsigned short *>(psa + 8 * SR + 8 * c));
+        }
+    };
+    const uint8_t *pqa = Q, *psa = S;
+    bool va = false, vb = false;
+    auto prologue = [&]() {
+        if constexpr (KC > 0) {
+            bases(0, pqa, psa, va, vb);
+#pragma unroll
+            for (int c = 0; c < kNB; ++c)
+                load(c, pqa, psa, va, vb, c);
+        }
+    };
+    // A head the caller marked static starts streaming before the wait for
+    // the preceding kernel on the stream; otherwise after it.
+    if (a.head_static)
+        prologue();
     pdl_wait();
 
-    // Largest |h| (bf16 magnitudes order like their bit patterns).
-    if (tid == 0)
-        s_hmax = 0u;
-    __syncthreads();
-    {
+    // Stage h as f16, scaled by 2^shift so that max|h| * 2^shift lies in
+    // [2^14, 2^15): hmax = f * 2^e with f in [0.5, 1), e = bf16 exponent
+    // field - 126 (bf16 magnitudes order like their bit patterns).
+    auto shift_of = [](unsigned int hmax) {
+        const int ef = (int)(hmax >> 7);
+        const int sh = hmax == 0u ? 0 : (ef == 0 ? 100 : 15 - (ef - 126));
+        return min(max(sh, -100), 100);
+    };
+    auto to_f16 = [](const uint4 &x, float up) {
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+        uint32_t hv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half2 hh = __floats2half2_rn(bf16_lo(xs[j]) * up, bf16_hi(xs[j]) * up);
+            hv[j] = *reinterpret_cast<const uint32_t *>(&hh);
+        }
+        return make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    };
+    auto block_max = [&](unsigned int mx) {
+        for (int off = 16; off >= 1; off >>= 1)
+            mx = max(mx, __shfl_xor_sync(kFull, mx, off));
+        if (lane == 0)
+            s_wmax[warp] = mx;
+    };
+    auto read_max = [&]() {
+        unsigned int mx = 0u;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            mx = max(mx, s_wmax[w]);
+        return mx;
+    };
+    // unit i = h[gg][k0 .. k0 + 8], ordered [chunk][u][g][q] (see above)
+    auto unit_k0 = [](int i, int &gg) {
+        const int qq = i & 3, r = i >> 2;
+        gg = r % M;
+        const int u = (r / M) & 3, c = r / (M * 4);
+        return kChunk * c + 32 * qq + 8 * u;
+    };
+    int shift;
+    for (int i = tid; i < M * kLists * KM; i += kThreads)
+        s_cand[i] = 0ull;
+    if constexpr (KC > 0) {
+        // one pass: every unit loaded once, its maximum taken, then stored
+        constexpr int kUnits = (KC / kChunk) * 16 * M;
+        constexpr int kPer = (kUnits + kThreads - 1) / kThreads;
+        uint4 hx[kPer];
+        unsigned int mx = 0u;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = tid + j * kThreads;
+            hx[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < kUnits) {
+                int gg;
+                const int k0 = unit_k0(i, gg);
+                hx[j] = __ldg(reinterpret_cast<const uint4 *>(a.h + (size_t)gg * KC + k0));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const uint32_t xs[4] = {hx[j].x, hx[j].y, hx[j].z, hx[j].w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                mx = max(mx, max(xs[t] & 0x7fffu, (xs[t] >> 16) & 0x7fffu));
+        }
+        block_max(mx);
+        __syncthreads();
+        shift = shift_of(read_max());
+        const float up = shift >= 0 ? pow2f(min(shift, 127)) : pow2f(max(shift, -126));
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = tid + j * kThreads;
+            if (i < kUnits)
+                s_h[i] = to_f16(hx[j], up);
+        }
+    } else {
+        // two passes over h from L2: the maximum, then the staging
         unsigned int mx = 0u;
         for (int i = tid; i < M * K / 2; i += kThreads) {
             const uint32_t x = __ldg(reinterpret_cast<const uint32_t *>(a.h) + i);
             mx = max(mx, max(x & 0x7fffu, (x >> 16) & 0x7fffu));
         }
-        for (int off = 16; off >= 1; off >>= 1)
-            mx = max(mx, __shfl_xor_sync(kFull, mx, off));
-        if (lane == 0)
-            atomicMax(&s_hmax, mx);
-    }
-    for (int i = tid; i < M * kLists * KM; i += kThreads)
-        s_cand[i] = 0ull;
-    __syncthreads();
-    if (tid == 0) {
-        // shift so that max|h| * 2^shift lies in [2^14, 2^15)
-        // hmax = f * 2^e with f in [0.5, 1): e = biased exponent - 126
-        const int ef = (int)(s_hmax >> 7);  // exponent field of the bf16
-        const int sh = s_hmax == 0u ? 0 : (ef == 0 ? 100 : 15 - (ef - 126));
-        s_shift = min(max(sh, -100), 100);
-    }
-    __syncthreads();
-    const int shift = s_shift;
-    {
+        block_max(mx);
+        __syncthreads();
+        shift = shift_of(read_max());
         const float up = shift >= 0 ? pow2f(min(shift, 127)) : pow2f(max(shift, -126));
         const int nunits = C * 4 * M * 4;
         for (int i = tid; i < nunits; i += kThreads) {
-            const int qq = i & 3, r = i >> 2;
-            const int gg = r % M, u = (r / M) & 3, c = r / (M * 4);
-            const int k0 = kChunk * c + 32 * qq + 8 * u;
-            uint32_t hv[4] = {0u, 0u, 0u, 0u};
-            if (k0 < K) {
-                const uint4 x = __ldg(reinterpret_cast<const uint4 *>(a.h + (size_t)gg * K + k0));
-                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const __half2 hh = __floats2half2_rn(bf16_lo(xs[j]) * up, bf16_hi(xs[j]) * up);
-                    hv[j] = *reinterpret_cast<const uint32_t *>(&hh);
-                }
-            }
-            s_h[i] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            int gg;
+            const int k0 = unit_k0(i, gg);
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (k0 < K)
+                x = __ldg(reinterpret_cast<const uint4 *>(a.h + (size_t)gg * K + k0));
+            s_h[i] = to_f16(x, up);
         }
     }
     __syncthreads();
+    if (!a.head_static)
+        prologue();
     const float down = (shift >= 0 ? pow2f(max(-shift, -126)) : pow2f(min(-shift, 127))) * a.gscale;
-
-    // Warps take 16-row groups round robin over the whole grid.
-    const int ngroups = (a.N + kRows - 1) / kRows;
-    const int GW = gridDim.x * kWarps;
-    const int gw = blockIdx.x * kWarps + warp;
-    const int my_groups = gw < ngroups ? (ngroups - 1 - gw) / GW + 1 : 0;
-    const int total = my_groups * C;
 
     TopList<KM> best0, best1;  // hidden rows 2q and 2q + 1
     best0.init();
@@ -226,13 +324,13 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
             d[j] = (acc[0][j] + acc[1][j]) + (acc[2][j] + acc[3][j]);
             acc[0][j] = acc[1][j] = acc[2][j] = acc[3][j] = 0.f;
         }
-        if (ra < a.N) {
+        if (ra < rend) {
             if (2 * q < M)
                 best0.insert(make_key(d[0] * down, ida));
             if (2 * q + 1 < M)
                 best1.insert(make_key(d[1] * down, ida));
         }
-        if (rb < a.N) {
+        if (rb < rend) {
             if (2 * q < M)
                 best0.insert(make_key(d[2] * down, idb));
             if (2 * q + 1 < M)
@@ -240,50 +338,18 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
         }
     };
     auto row_id = [&](int r) {
-        return r < a.N ? (a.d2t ? __ldg(a.d2t + r) : (int)(a.id_base + r)) : 0;
+        return r < rend ? (a.d2t ? __ldg(a.d2t + r) : (int)(a.id_base + r)) : 0;
     };
 
     if constexpr (KC > 0) {
         // ---- compile-time K: one base pointer per group, immediate offsets ----
         constexpr int CC = KC / kChunk;
         static_assert(CC % kNB == 0, "the ring must divide the chunks");
-        constexpr int QR = KC / 2, SR = KC / 16;  // bytes per row: codes, scales
-        uint4 bqa[kNB], bqb[kNB];
-        uint32_t bsa[kNB], bsb[kNB];
-#pragma unroll
-        for (int b2 = 0; b2 < kNB; ++b2) {
-            bqa[b2] = bqb[b2] = make_uint4(0u, 0u, 0u, 0u);
-            bsa[b2] = bsb[b2] = 0u;
-        }
-        // a group's lane bases: codes of rows ra / rb at byte 16 q, scales at 2 q
-        auto bases = [&](int li, const uint8_t *&pqa, const uint8_t *&psa, bool &va, bool &vb) {
-            const int ra = (gw + li * GW) * kRows + g;
-            va = li < my_groups && ra < a.N;
-            vb = li < my_groups && ra + 8 < a.N;
-            pqa = Q + (size_t)ra * QR + 16 * q;
-            psa = S + (size_t)ra * SR + 2 * q;
-        };
-        auto load = [&](int b2, const uint8_t *pqa, const uint8_t *psa, bool va, bool vb, int c) {
-            if (va) {
-                bqa[b2] = ld_stream16(pqa + 64 * c);
-                bsa[b2] = __ldg(reinterpret_cast<const unsigned short *>(psa + 8 * c));
-            }
-            if (vb) {
-                bqb[b2] = ld_stream16(pqa + 8 * QR + 64 * c);
-                bsb[b2] = __ldg(reinterpret_cast<const unsigned short *>(psa + 8 * SR + 8 * c));
-            }
-        };
-        const uint8_t *pqa, *psa;
-        bool va, vb;
-        bases(0, pqa, psa, va, vb);
-#pragma unroll
-        for (int c = 0; c < kNB; ++c)
-            load(c, pqa, psa, va, vb, c);
         for (int li = 0; li < my_groups; ++li) {
             const uint8_t *nqa, *nsa;
             bool nva, nvb;
             bases(li + 1, nqa, nsa, nva, nvb);
-            const int ra = (gw + li * GW) * kRows + g;
+            const int ra = row0 + li * kRows + g;
             const int ida = row_id(ra), idb = row_id(ra + 8);
 #pragma unroll
             for (int c = 0; c < CC; ++c) {
@@ -303,24 +369,21 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
     } else {
         // ---- run-time K: one flat (group, chunk) stream, predicated ----
         const int total = my_groups * C;
-        uint4 bqa[kNB], bqb[kNB];
-        uint32_t bsa[kNB], bsb[kNB];
         int li = 0, lc = 0;  // load cursor (my group index, chunk)
         auto issue = [&](int b2) {
-            const int grp = gw + li * GW;
-            const int ra = grp * kRows + g, rb = ra + 8;
+            const int ra = row0 + li * kRows + g, rb = ra + 8;
             const int kc = kChunk * lc + 32 * q;
             const bool kin = li < my_groups && kc < K;
             bqa[b2] = make_uint4(0u, 0u, 0u, 0u);
             bqb[b2] = make_uint4(0u, 0u, 0u, 0u);
             bsa[b2] = 0u;
             bsb[b2] = 0u;
-            if (kin && ra < a.N) {
+            if (kin && ra < rend) {
                 bqa[b2] = ld_stream16(Q + (size_t)ra * qrow + kc / 2);
                 bsa[b2] = __ldg(
                     reinterpret_cast<const unsigned short *>(S + (size_t)ra * srow + kc / 16));
             }
-            if (kin && rb < a.N) {
+            if (kin && rb < rend) {
                 bqb[b2] = ld_stream16(Q + (size_t)rb * qrow + kc / 2);
                 bsb[b2] = __ldg(
                     reinterpret_cast<const unsigned short *>(S + (size_t)rb * srow + kc / 16));
@@ -338,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
 #pragma unroll
             for (int b2 = 0; b2 < kNB; ++b2) {
                 if (t0 + b2 < total) {
-                    const int ra = (gw + ci * GW) * kRows + g;
+                    const int ra = row0 + ci * kRows + g;
                     if (cc == 0) {
                         ida = row_id(ra);
                         idb = row_id(ra + 8);
@@ -387,11 +450,11 @@ cudaError_t launch_one(const ArgmaxArgs &a, cudaStream_t s)
         return cudaErrorInvalidConfiguration;
     if (per_sm > 2)
         per_sm = 2;
-    const long long groups = ((long long)a.N + kRows - 1) / kRows;
     long long grid = (long long)di.sms * per_sm;
-    const long long max_by_groups = (groups + kWarps - 1) / kWarps;  // >= 1 group per warp
-    if (grid > max_by_groups)
-        grid = max_by_groups;
+    // at least half an MMA tile of rows per warp on average
+    const long long max_by_rows = ((long long)a.N + kWarps * 8 - 1) / (kWarps * 8);
+    if (grid > max_by_rows)
+        grid = max_by_rows;
     if (grid > kMaxCtas)
         grid = kMaxCtas;
     if (grid < 1)
