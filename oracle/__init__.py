@@ -81,6 +81,11 @@ def _load():
     lib.oracle_logits_nvfp4.argtypes = [p, p, ctypes.c_float, i64, i64, p, i64, p,
                                         ctypes.c_int]
     lib.oracle_logits_nvfp4.restype = ctypes.c_int
+    lib.oracle_score_ids_bf16.argtypes = [p, i64, i64, i64, p, i64, p, i64, p]
+    lib.oracle_score_ids_bf16.restype = None
+    lib.oracle_score_ids_nvfp4.argtypes = [p, p, ctypes.c_float, i64, i64, i64, p, i64, p,
+                                           i64, p]
+    lib.oracle_score_ids_nvfp4.restype = None
     lib.oracle_topk.argtypes = [p, i64, i64, p, ctypes.c_int, p, p, p]
     lib.oracle_topk.restype = None
     lib.oracle_check_trim.argtypes = [p, i64, i64, p, i64, p, p]
@@ -149,6 +154,42 @@ def logits_nvfp4(q: np.ndarray, scales: np.ndarray, g: float, h: np.ndarray,
     t = _load().oracle_logits_nvfp4(_ptr(q), _ptr(scales), float(g), N, K, _ptr(h),
                                     M, _ptr(out), nthreads)
     return out, int(t)
+
+
+def score_ids_bf16(w: np.ndarray, h: np.ndarray, ids: np.ndarray, id_base: int = 0):
+    """fp32 scores[M][c]: the logit of head row ids[m][j] - id_base against
+    h[m] (the same dot as logits_bf16); NaN for an id outside the head."""
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    N, K = w.shape
+    M = h.shape[0]
+    assert h.shape[1] == K and ids.ndim == 2 and ids.shape[0] == M
+    c = ids.shape[1]
+    out = np.empty((M, c), dtype=np.float32)
+    _load().oracle_score_ids_bf16(_ptr(w), N, K, int(id_base), _ptr(h), M, _ptr(ids), c,
+                                  _ptr(out))
+    return out
+
+
+def score_ids_nvfp4(q: np.ndarray, scales: np.ndarray, g: float, h: np.ndarray,
+                    ids: np.ndarray, id_base: int = 0):
+    """score_ids_bf16 for an NVFP4 head (the same weight decode as
+    logits_nvfp4)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    N, Kh = q.shape
+    K = 2 * Kh
+    assert scales.shape == (N, K // 16)
+    M = h.shape[0]
+    assert h.shape[1] == K and ids.ndim == 2 and ids.shape[0] == M
+    c = ids.shape[1]
+    out = np.empty((M, c), dtype=np.float32)
+    _load().oracle_score_ids_nvfp4(_ptr(q), _ptr(scales), float(g), N, K, int(id_base),
+                                   _ptr(h), M, _ptr(ids), c, _ptr(out))
+    return out
 
 
 def nvfp4_weight(q, scales, g, n, k) -> float:

@@ -28,6 +28,10 @@
  *       requantizing the trimmed head to NVFP4).  The layout (row-major
  *       codes, low nibble = even k, one e4m3 scale per 16 consecutive k of a
  *       row, one fp32 tensor scale) is the reading this project adopts.
+ *   candidate scores: logit[m][j] = the same dot for head row
+ *       ids[m][j] - id_base, NaN for an id outside the head's rows ("Masked
+ *       MTP drafts", section "Update (November 2026)": a drafter's candidates
+ *       scored through the target's own LM head, bf16 or NVFP4).
  *   trim check: W_trim[i] == W_full[ranks[i]] byte for byte, d2t[i] ==
  *       ranks[i] ("Masked MTP drafts": a ranks list next to the model, the
  *       head weight trimmed at load).
@@ -126,28 +130,33 @@ typedef struct {
     int64_t n_begin, n_end;
 } logit_job;
 
+/* One logit: head row n against hidden row hm, ascending k in fp32. */
+static float row_dot(const logit_job *j, int64_t n, const uint16_t *hm)
+{
+    float acc = 0.0f;
+    if (j->kind == 0) {
+        const uint16_t *wn = j->w_bf16 + n * j->K;
+        for (int64_t k = 0; k < j->K; ++k) {
+            float prod = oracle_bf16_to_f32(wn[k]) * oracle_bf16_to_f32(hm[k]);
+            acc = acc + prod;
+        }
+    } else {
+        for (int64_t k = 0; k < j->K; ++k) {
+            float w = oracle_nvfp4_weight(j->q, j->scales, j->g, j->K, n, k);
+            float prod = w * oracle_bf16_to_f32(hm[k]);
+            acc = acc + prod;
+        }
+    }
+    return acc;
+}
+
 static void *logit_worker(void *arg)
 {
     logit_job *j = (logit_job *)arg;
     for (int64_t m = 0; m < j->M; ++m) {
         const uint16_t *hm = j->h + m * j->K;
-        for (int64_t n = j->n_begin; n < j->n_end; ++n) {
-            float acc = 0.0f;
-            if (j->kind == 0) {
-                const uint16_t *wn = j->w_bf16 + n * j->K;
-                for (int64_t k = 0; k < j->K; ++k) {
-                    float prod = oracle_bf16_to_f32(wn[k]) * oracle_bf16_to_f32(hm[k]);
-                    acc = acc + prod;
-                }
-            } else {
-                for (int64_t k = 0; k < j->K; ++k) {
-                    float w = oracle_nvfp4_weight(j->q, j->scales, j->g, j->K, n, k);
-                    float prod = w * oracle_bf16_to_f32(hm[k]);
-                    acc = acc + prod;
-                }
-            }
-            j->logits[m * j->N + n] = acc;
-        }
+        for (int64_t n = j->n_begin; n < j->n_end; ++n)
+            j->logits[m * j->N + n] = row_dot(j, n, hm);
     }
     return NULL;
 }
@@ -223,6 +232,54 @@ int oracle_logits_nvfp4(const uint8_t *q, const uint8_t *scales, float g, int64_
     j.h = h;
     j.logits = logits;
     return run_logits(j, nthreads);
+}
+
+/* ------------------------------------------------------------------ */
+/* Candidate scores: the dot of the head row each id names.            */
+/* ------------------------------------------------------------------ */
+
+static void score_ids(const logit_job *j, int64_t id_base, const int32_t *ids, int64_t c,
+                      float *out)
+{
+    for (int64_t m = 0; m < j->M; ++m) {
+        const uint16_t *hm = j->h + m * j->K;
+        for (int64_t t = 0; t < c; ++t) {
+            int64_t n = (int64_t)ids[m * c + t] - id_base;
+            out[m * c + t] = (n >= 0 && n < j->N) ? row_dot(j, n, hm) : NAN;
+        }
+    }
+}
+
+void oracle_score_ids_bf16(const uint16_t *w, int64_t N, int64_t K, int64_t id_base,
+                           const uint16_t *h, int64_t M, const int32_t *ids, int64_t c,
+                           float *out)
+{
+    logit_job j;
+    memset(&j, 0, sizeof j);
+    j.kind = 0;
+    j.w_bf16 = w;
+    j.N = N;
+    j.K = K;
+    j.M = M;
+    j.h = h;
+    score_ids(&j, id_base, ids, c, out);
+}
+
+void oracle_score_ids_nvfp4(const uint8_t *q, const uint8_t *scales, float g, int64_t N,
+                            int64_t K, int64_t id_base, const uint16_t *h, int64_t M,
+                            const int32_t *ids, int64_t c, float *out)
+{
+    logit_job j;
+    memset(&j, 0, sizeof j);
+    j.kind = 1;
+    j.q = q;
+    j.scales = scales;
+    j.g = g;
+    j.N = N;
+    j.K = K;
+    j.M = M;
+    j.h = h;
+    score_ids(&j, id_base, ids, c, out);
 }
 
 /* ------------------------------------------------------------------ */
