@@ -51,7 +51,8 @@ def parse():
     p.add_argument("--repeats", type=int, default=5)
     p.add_argument("--profile", nargs="?", const="c2m1", default=None,
                    help="only warm-up + timed calls of one workload, for ncu captures: "
-                        "c2m1 (default), c2m3, c1m1, c1m3, c3m1, c4m8, c4m16, c4m32, c5m1, c5m3")
+                        "c2m1 (default), c2m3, c1m1, c1m3, c3m1, c4m8, c4m16, c4m32, c5m1, c5m3, "
+                        "scm16 (candidate scores, 16 rows x 32 through the c2 head)")
     return p.parse_args()
 
 
@@ -293,6 +294,17 @@ def run_profile(args):
         wl = S.c5(Ms=(M,))
         head = dvl.Head(dev(torch, wl.q), scales=dev(torch, wl.scales), global_scale=wl.g,
                         V=wl.V, d2t=dev(torch, wl.d2t), static=True)
+    elif cfg == "sc":
+        # candidate scores through the full c2 head: M hidden rows x 32
+        wl = S.c2(Ms=())
+        head = dvl.Head(dev(torch, wl.w), V=wl.V, static=True)
+        h = dev(torch, S.hidden_bf16(91, M, wl.K))
+        cands = dev(torch, S.candidate_ids(92, wl.V, M, 32))
+        for _ in range(max(3, args.warmup) + args.steps):
+            dvl.score_ids(head, h, cands)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_run": name, "launches": max(3, args.warmup) + args.steps}))
+        return
     else:
         raise SystemExit(f"unknown profile workload {name}")
     h = dev(torch, wl.h[M])
@@ -469,6 +481,27 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
     t = repeat_stats(torch, lambda i: g.replay(), 4, R)
     out["c2_full_M1_argmax_graph50"] = entry(RL.call_bytes(N2, K2, 1), t[0] / 50, t[1] / 50,
                                              t[2] / 50, peak)
+    # candidate scores through the full head: 16 hidden rows x 32 candidates,
+    # 160 Zipf-drawn candidate sets cycled call to call (frequent ids recur
+    # across sets, as they do from one decoding step to the next)
+    Ms, cs = 16, 32
+    hsc = dev(torch, S.hidden_bf16(91, Ms, K2))
+    cands = [dev(torch, S.candidate_ids(1000 + i, N2, Ms, cs)) for i in range(160)]
+    sc_out = torch.empty((Ms, cs), dtype=torch.float32, device="cuda")
+    t = repeat_stats(torch, lambda i: dvl.score_ids(head2, hsc, cands[i % 160], logits=sc_out),
+                     n_calls, R)
+    out["c2_scores_M16_c32"] = entry(RL.score_bytes(Ms, cs, K2), *t, peak,
+                                     {"note": "gather-GEMV, memory-latency bound; 160 candidate "
+                                              "sets cycled"})
+    gsc = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gsc):
+        for i in range(40):
+            dvl.score_ids(head2, hsc, cands[i % 160], logits=sc_out)
+    t = repeat_stats(torch, lambda i: gsc.replay(), 4, R)
+    out["c2_scores_M16_c32_graph40"] = entry(RL.score_bytes(Ms, cs, K2), t[0] / 40, t[1] / 40,
+                                             t[2] / 40, peak, {"note": "CUDA-graph replay, 40 "
+                                                               "calls, 40 candidate sets"})
+    del cands, gsc
 
     # 16k shortlist (trim vs full) with L2 rotation
     wl1 = S.c1()

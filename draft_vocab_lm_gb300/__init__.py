@@ -13,6 +13,7 @@ not built.
     head = Head(w, V=248_320, d2t=d2t)            # w: CUDA bf16 [N][K]
     ids, logits = draft_argmax(head, h)            # h: CUDA bf16 [M][K]
     ids, logits = draft_topk(head, h, k=4)
+    logits = score_ids(head, h, cand)              # cand: CUDA int32 [M][c]
     w_trim, _, d2t, n_dup = trim_head(w_full, ranks)
 """
 from __future__ import annotations
@@ -26,7 +27,7 @@ from ._native import (DVL_BF16, DVL_HEAD_STATIC, DVL_K_MULTIPLE, DVL_MAX_K, DVL_
                       DVL_MAX_TOPK, DVL_NVFP4, DvlError, DvlHead, check, lib)
 
 __all__ = [
-    "Head", "DvlError", "draft_argmax", "draft_topk", "trim_head", "workspace_bytes",
+    "Head", "DvlError", "draft_argmax", "draft_topk", "score_ids", "trim_head", "workspace_bytes",
     "make_workspace", "workspace_init", "histogram", "build_ranks", "union_sorted",
     "read_ranks_txt", "write_ranks_txt", "roofline", "version",
 ]
@@ -193,6 +194,25 @@ def draft_argmax(head: Head, h, *, ids=None, logits=None, ws=None, stream=None):
                                  logits.data_ptr(), ws.data_ptr(), ws.numel(),
                                  _stream_handle(stream, h.device)))
     return ids, logits
+
+
+def score_ids(head: Head, h, ids, *, logits=None, stream=None):
+    """Per hidden row m and candidate j: the logit of the head row that
+    ids[m][j] names (ids id_base .. id_base + N - 1; NaN outside).  The head
+    has no d2t; ids is a CUDA int32 [M][c] tensor."""
+    torch = _torch()
+    _check_h(head, h)
+    M = h.shape[0]
+    if (not ids.is_cuda or ids.dtype != torch.int32 or ids.dim() != 2
+            or not ids.is_contiguous() or ids.shape[0] != M):
+        raise ValueError("ids must be a contiguous CUDA int32 [M][c] tensor")
+    c = ids.shape[1]
+    if logits is None:
+        logits = torch.empty((M, c), dtype=torch.float32, device=h.device)
+    check("dvl_score_ids",
+          lib().dvl_score_ids(ctypes.byref(head.struct()), h.data_ptr(), M, ids.data_ptr(), c,
+                              logits.data_ptr(), _stream_handle(stream, h.device)))
+    return logits
 
 
 def trim_head(w_full, ranks, *, scales=None, stream=None):

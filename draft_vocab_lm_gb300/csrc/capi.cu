@@ -249,6 +249,34 @@ dvl_status dvl_draft_topk(const dvl_head *head, const void *h, int32_t M, int32_
     return reduce_call(head, h, M, k, ids, logits, ws, ws_bytes, stream);
 }
 
+dvl_status dvl_score_ids(const dvl_head *head, const void *h, int32_t M, const int32_t *ids,
+                         int32_t c, float *logits, void *stream)
+{
+    dvl_status st = check_head(head);
+    if (st != DVL_OK)
+        return st;
+    if (head->d2t || M < 1 || M > DVL_MAX_M || c < 1 || (int64_t)M * c > 0x7fffffffLL)
+        return DVL_ERR_INVALID_ARG;
+    if (!h || !aligned(h, 16) || !ids || !aligned(ids, 4) || !logits || !aligned(logits, 4))
+        return DVL_ERR_INVALID_ARG;
+    ScoreArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.dtype = head->dtype;
+    a.w = head->w;
+    a.scales = head->scales;
+    a.gscale = head->global_scale;
+    a.id_base = head->id_base;
+    a.N = head->N;
+    a.K = head->K;
+    a.M = M;
+    a.c = c;
+    a.h = static_cast<const uint16_t *>(h);
+    a.ids = ids;
+    a.out = logits;
+    cudaError_t e = launch_score(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DVL_OK : cuda_failed(e);
+}
+
 dvl_status dvl_trim_head(const dvl_head *full, const int32_t *ranks, int32_t n_ranks,
                          void *w_trim, uint8_t *scales_trim, int32_t *d2t,
                          int32_t *n_duplicates, void *stream)

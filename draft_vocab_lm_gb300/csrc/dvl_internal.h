@@ -61,6 +61,21 @@ int max_chunk_rows_nvfp4(int K);
 dvl_status check_reduce_args(const dvl_head *hd, const void *h, int32_t M, int32_t k,
                              const void *ids, const void *logits);
 
+// Arguments of a candidate-scoring launch: out[m][j] = W[ids[m][j] - id_base]
+// . h[m] for m < M, j < c (NaN for an id outside the head's N rows).
+struct ScoreArgs {
+    int dtype;                // DVL_BF16 or DVL_NVFP4
+    const void *w;            // bf16 [N][K] or NVFP4 codes [N][K/2]
+    const uint8_t *scales;    // NVFP4 E4M3 [N][K/16]
+    float gscale;             // NVFP4 tensor scale
+    int64_t id_base;          // id of row 0
+    int N, K, M, c;
+    const uint16_t *h;        // bf16 [M][K]
+    const int32_t *ids;       // [M][c]
+    float *out;               // [M][c]
+};
+cudaError_t launch_score(const ScoreArgs &a, cudaStream_t s);
+
 cudaError_t launch_trim_rows(const unsigned char *src, int64_t src_row_bytes,
                              unsigned char *dst, const int32_t *ranks, int n,
                              cudaStream_t s);

@@ -32,6 +32,14 @@ def call_bytes(N: int, K: int, M: int, dtype: str = "bf16", k: int = 1) -> int:
     return head_bytes(N, K, dtype) + M * K * 2 + M * k * 12
 
 
+def score_bytes(M: int, c: int, K: int, dtype: str = "bf16") -> int:
+    """Algorithmic bytes of one candidate-scoring call: each named head row
+    (M*c rows, repeats counted once per candidate), the hidden rows, the ids
+    and the fp32 scores."""
+    row = head_bytes(1, K, dtype) - (4 if dtype == "nvfp4" else 0)
+    return M * c * row + M * K * 2 + M * c * 8
+
+
 def call_flops(N: int, K: int, M: int) -> int:
     """Multiply-adds of the projection, counted as 2 flops each."""
     return 2 * M * N * K

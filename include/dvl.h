@@ -190,6 +190,28 @@ dvl_status dvl_draft_topk(const dvl_head *head, const void *h, int32_t M, int32_
 dvl_status dvl_draft_argmax_noalloc(const dvl_head *head, const void *h, int32_t M,
                                     int32_t *ids, float *max_logit, void *stream);
 
+/* Candidate scores through a head ("Masked MTP drafts", section "Update
+ * (November 2026)": a drafter that carries no head of its own scores its
+ * candidates through the target's LM head, bf16 or NVFP4, and the trim
+ * stacks on top).  For m < M and j < c:
+ *   logits[m][j] = sum_k W[ids[m][j] - id_base][k] * h[m][k]
+ * with the head's dtype and arithmetic (fp32 accumulation; NVFP4 weights
+ * e2m1 * e4m3 with the tensor scale on the finished dot), in any summation
+ * order.  The head's rows are ids id_base .. id_base + N - 1: a full head
+ * (id_base 0) or any contiguous slice of one.  An id outside them scores
+ * NaN; the ids live on the device and are not checked on the host.
+ *   head:   a head without d2t (d2t == NULL).
+ *   h:      device bf16 [M][K], row-major, 16-byte aligned.
+ *   M:      1 .. DVL_MAX_M.
+ *   ids:    device int32 [M][c], row-major (the candidates of row m).
+ *   c:      candidates per row, >= 1, with M * c < 2^31.
+ *   logits: device fp32 [M][c] (out), row-major.
+ * Nothing is allocated; no workspace.  The call is enqueued on `stream`.
+ * Errors: DVL_ERR_INVALID_ARG (the head checks of dvl_draft_argmax, a head
+ * with d2t, NULL or misaligned pointers, M or c out of range), DVL_ERR_CUDA. */
+dvl_status dvl_score_ids(const dvl_head *head, const void *h, int32_t M,
+                         const int32_t *ids, int32_t c, float *logits, void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* Load time                                                              */
 /* ---------------------------------------------------------------------- */

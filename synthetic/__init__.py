@@ -182,6 +182,29 @@ def zipf_tokens(seed: int, V: int, S: int, s: float = 1.1, tag: int = 3) -> np.n
     return out
 
 
+def candidate_ids(seed: int, V: int, M: int, c: int, s: float = 1.1, tag: int = 5) -> np.ndarray:
+    """A drafter's candidates: for each of M rows, c distinct ids drawn from
+    the bounded Zipf(s) law of zipf_tokens (frequent tokens are likely
+    candidates).  Returns int32[M][c]."""
+    rng = np.random.default_rng([seed, tag])
+    perm = zipf_permutation(seed, V, tag)
+    p = np.arange(1, V + 1, dtype=np.float64) ** (-s)
+    cdf = np.cumsum(p)
+    cdf /= cdf[-1]
+    out = np.empty((M, c), dtype=np.int32)
+    for m in range(M):
+        got: list[int] = []
+        seen: set[int] = set()
+        while len(got) < c:
+            r = np.minimum(np.searchsorted(cdf, rng.random(2 * c), side="right"), V - 1)
+            for x in perm[r].tolist():
+                if x not in seen and len(got) < c:
+                    seen.add(x)
+                    got.append(x)
+        out[m] = got
+    return out
+
+
 def union_sets(seed: int, V: int, na: int, nb: int, n_shared: int):
     """Two id sets A (|A| = na) and B (|B| = nb) with |A & B| = n_shared, drawn
     without replacement from [0, V).  Returns (A, B) as unsorted int32."""

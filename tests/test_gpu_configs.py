@@ -3,7 +3,8 @@ library calls (and so the same launch configuration) the benchmark times,
 against the oracle run in full on every row.
 
 c1  16,000-row shortlist of a 248,320 x 2,560 head (trim, then argmax, M=1)
-c2  the full 248,320 x 2,560 head, M in {1, 3}, argmax and top-4
+c2  the full 248,320 x 2,560 head, M in {1, 3}, argmax and top-4; candidate
+    scores of 16 hidden rows x 32 candidates through it
 c3  32,768-row FR-Spec trim of a 248,320 x 5,120 head, ranks built on the
     host from a Zipf token stream, M in {1, 2, 3, 4}
 c4  52,755-row union list, M in {8, 16, 32}, planted near-ties
@@ -66,6 +67,28 @@ def test_c1_shortlist16k(dvl, oracle_mod):
 def c2(dvl):
     wl = S.c2()
     return wl, dvl.Head(dev(wl.w), V=wl.V)
+
+
+def test_c2_candidate_scores(dvl, oracle_mod, c2):
+    # candidate scoring through the full head, in the benchmark's shape: 16
+    # hidden rows x 32 Zipf-drawn candidates; every score against the oracle
+    # within twice the fp32 summation bound (both sides sum exact products)
+    wl, head = c2
+    M, c = 16, 32
+    h = S.hidden_bf16(91, M, wl.K)
+    ids = S.candidate_ids(92, wl.V, M, c)
+    got = dvl.score_ids(head, dev(h), dev(ids)).cpu().numpy()
+    want = oracle_mod.score_ids_bf16(wl.w, h, ids)
+    hf = S.bf16_bits_to_f32(h).astype(np.float64)
+    worst = 0.0
+    for m in range(M):
+        for j in range(c):
+            prod = S.bf16_bits_to_f32(wl.w[ids[m, j]]).astype(np.float64) * hf[m]
+            bound = 2 * (wl.K - 1) * 2.0 ** -24 * np.abs(prod).sum()
+            err = abs(float(got[m, j]) - float(want[m, j]))
+            assert err <= bound
+            worst = max(worst, err / bound)
+    report("c2 scores 16x32", {"pairs": M * c, "worst err / bound": round(worst, 4)})
 
 
 @pytest.mark.parametrize("M", [1, 3])

@@ -149,3 +149,29 @@ def test_trim_checks_reject_bad_ranks_before_any_launch(dvl):
     assert L.dvl_trim_head(ctypes.byref(h), neg, 1, 0x1000, None, 0x2000, None, None) == 2
     sliced = _head(N=50)  # not a full head
     assert L.dvl_trim_head(ctypes.byref(sliced), ranks, 1, 0x1000, None, 0x2000, None, None) == 1
+
+
+@pytest.mark.parametrize("bad", [
+    dict(dtype=7), dict(N=0), dict(K=100), dict(flags=2), dict(w=None), dict(dtype=1),
+    dict(d2t=0x6000),
+])
+def test_score_checks_reject_bad_heads_before_any_launch(dvl, bad):
+    # a head with d2t has no row for an arbitrary full id: refused
+    from draft_vocab_lm_gb300._native import lib
+    L = lib()
+    h = _head(**bad)
+    assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 1, 0x2000, 4, 0x4000, None) == 1
+
+
+def test_score_shape_and_pointer_checks(dvl):
+    from draft_vocab_lm_gb300._native import lib
+    L = lib()
+    h = _head()
+    assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 0, 0x2000, 4, 0x4000, None) == 1
+    assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 33, 0x2000, 4, 0x4000, None) == 1
+    assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 1, 0x2000, 0, 0x4000, None) == 1
+    assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 32, 0x2000, 0x7fffffff, 0x4000, None) == 1
+    assert L.dvl_score_ids(ctypes.byref(h), 0x3008, 1, 0x2000, 4, 0x4000, None) == 1
+    assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 1, None, 4, 0x4000, None) == 1
+    assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 1, 0x2002, 4, 0x4000, None) == 1
+    assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 1, 0x2000, 4, None, None) == 1
