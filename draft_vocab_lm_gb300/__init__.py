@@ -27,7 +27,8 @@ from ._native import (DVL_BF16, DVL_HEAD_STATIC, DVL_K_MULTIPLE, DVL_MAX_K, DVL_
                       DVL_MAX_TOPK, DVL_NVFP4, DvlError, DvlHead, check, lib)
 
 __all__ = [
-    "Head", "DvlError", "draft_argmax", "draft_topk", "score_ids", "trim_head", "workspace_bytes",
+    "Head", "DvlError", "draft_argmax", "draft_topk", "score_ids", "trim_head", "learn_rows",
+    "Shortlist", "workspace_bytes",
     "make_workspace", "workspace_init", "histogram", "build_ranks", "union_sorted",
     "read_ranks_txt", "write_ranks_txt", "roofline", "version",
 ]
@@ -238,6 +239,89 @@ def trim_head(w_full, ranks, *, scales=None, stream=None):
                               d2t.data_ptr(), ctypes.byref(dup),
                               _stream_handle(stream, w_full.device)))
     return w_trim, s_trim, d2t, int(dup.value)
+
+
+def learn_rows(w_full, ids, w_trim, d2t, row0: int, *, scales=None, scales_trim=None,
+               stream=None) -> None:
+    """Copy the full head's rows `ids` (host ids) into rows row0 .. row0 + n - 1
+    of trimmed buffers and set their d2t entries (dvl_learn_rows).  The first
+    call on the stream afterwards must not treat the trimmed head as static;
+    Shortlist takes care of that."""
+    r = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    full = Head(w_full, scales=scales)
+    check("dvl_learn_rows",
+          lib().dvl_learn_rows(ctypes.byref(full.struct()), r.ctypes.data, r.shape[0], int(row0),
+                               w_trim.data_ptr(),
+                               scales_trim.data_ptr() if scales_trim is not None else None,
+                               d2t.data_ptr(), _stream_handle(stream, w_full.device)))
+
+
+class Shortlist:
+    """A trimmed head with spare rows that learns escaped ids while serving.
+
+    ("Masked MTP drafts", section "Update (November 2026)": a static trim can
+    miss; learning the escaped ids into spare head rows recovered the loss.)
+    The head is trimmed to `ranks` into buffers of `capacity` rows; learn()
+    appends the full head's rows of ids the list does not hold yet, in stream
+    order, until the spare rows run out.
+
+        sl = Shortlist(w_full, ranks, capacity=len(ranks) + 1024)
+        ids, logits = draft_argmax(sl.head(), h)
+        sl.learn(emitted_ids)        # host ids the target produced
+    """
+
+    def __init__(self, w_full, ranks, capacity: int, *, scales=None, global_scale: float = 1.0,
+                 stream=None):
+        torch = _torch()
+        r = np.ascontiguousarray(np.asarray(ranks, dtype=np.int32))
+        if capacity < r.shape[0]:
+            raise ValueError("capacity below the number of ranks")
+        self.V = w_full.shape[0]
+        self.capacity = int(capacity)
+        self.w_full, self.scales_full = w_full, scales
+        self.global_scale = float(global_scale)
+        self.stream = stream
+        self.w = torch.empty((capacity, w_full.shape[1]), dtype=w_full.dtype, device=w_full.device)
+        self.scales = None
+        if scales is not None:
+            self.scales = torch.empty((capacity, scales.shape[1]), dtype=scales.dtype,
+                                      device=scales.device)
+        self.d2t = torch.empty(capacity, dtype=torch.int32, device=w_full.device)
+        self.row_of = np.full(self.V, -1, dtype=np.int64)  # full id -> trimmed row
+        self.n = 0
+        self._pending = False
+        self._append(r)
+
+    def _append(self, ids: np.ndarray) -> None:
+        learn_rows(self.w_full, ids, self.w, self.d2t, self.n, scales=self.scales_full,
+                   scales_trim=self.scales, stream=self.stream)
+        fresh = self.row_of[ids] < 0
+        self.row_of[ids[fresh]] = self.n + np.nonzero(fresh)[0]
+        self.n += ids.shape[0]
+        self._pending = True
+
+    def learn(self, ids) -> np.ndarray:
+        """Learn the ids (host, any order, repeats allowed) the list does not
+        hold, as many as spare rows remain; returns the ids learned."""
+        x = np.asarray(ids, dtype=np.int64).ravel()
+        if x.size and (x.min() < 0 or x.max() >= self.V):
+            raise ValueError("ids outside the vocabulary")
+        x = x[self.row_of[x] < 0]
+        x = x[np.sort(np.unique(x, return_index=True)[1])]  # first occurrences, in order
+        x = x[:self.capacity - self.n].astype(np.int32)
+        if x.size:
+            self._append(x)
+        return x
+
+    def head(self, *, static: bool = True) -> Head:
+        """The active rows as a Head.  The first head handed out after a
+        learn is not static (the rows were written by the stream's latest
+        kernels); later ones are, unless static=False."""
+        hd = Head(self.w[:self.n], V=self.V, d2t=self.d2t[:self.n],
+                  scales=self.scales[:self.n] if self.scales is not None else None,
+                  global_scale=self.global_scale, static=static and not self._pending)
+        self._pending = False
+        return hd
 
 
 # ---------------------------------------------------------------------------

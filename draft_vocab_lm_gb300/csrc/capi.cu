@@ -195,6 +195,52 @@ dvl_status check_reduce_args(const dvl_head *hd, const void *h, int32_t M, int32
     return DVL_OK;
 }
 
+// Rows row0 .. row0 + n - 1 of a trimmed head from the full head's rows
+// ids[0 .. n - 1] (host ids, checked first), and d2t[row0 + i] = ids[i].
+static dvl_status gather_rows(const dvl_head *full, const int32_t *ids, int32_t n,
+                              int32_t row0, void *w_trim, uint8_t *scales_trim, int32_t *d2t,
+                              int32_t *n_duplicates, void *stream)
+{
+    dvl_status st = check_head(full);
+    if (st != DVL_OK)
+        return st;
+    if ((int64_t)full->N != full->V || full->d2t || full->id_base != 0)
+        return DVL_ERR_INVALID_ARG;
+    if (!ids || n < 1 || row0 < 0 || (int64_t)row0 + n > 0x7fffffffLL)
+        return DVL_ERR_INVALID_ARG;
+    if (!w_trim || !aligned(w_trim, 16) || !d2t || !aligned(d2t, 4))
+        return DVL_ERR_INVALID_ARG;
+    if (full->dtype == DVL_NVFP4 && (!scales_trim || !aligned(scales_trim, 16)))
+        return DVL_ERR_INVALID_ARG;
+    std::vector<unsigned char> seen((size_t)full->V, 0);
+    int32_t dup = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t r = ids[i];
+        if (r < 0 || (int64_t)r >= full->V)
+            return DVL_ERR_OUT_OF_RANGE;
+        if (seen[(size_t)r])
+            ++dup;
+        seen[(size_t)r] = 1;
+    }
+    if (n_duplicates)
+        *n_duplicates = dup;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t *d2t_rows = d2t + row0;
+    cudaError_t e =
+        cudaMemcpyAsync(d2t_rows, ids, (size_t)n * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess)
+        return cuda_failed(e);
+    const int64_t K = full->K;
+    const int64_t wrow = full->dtype == DVL_BF16 ? K * 2 : K / 2;
+    e = launch_trim_rows(static_cast<const unsigned char *>(full->w), wrow,
+                         static_cast<unsigned char *>(w_trim) + (int64_t)row0 * wrow, d2t_rows, n,
+                         s);
+    if (e == cudaSuccess && full->dtype == DVL_NVFP4)
+        e = launch_trim_rows(full->scales, K / 16, scales_trim + (int64_t)row0 * (K / 16),
+                             d2t_rows, n, s);
+    return e == cudaSuccess ? DVL_OK : cuda_failed(e);
+}
+
 }  // namespace dvl
 
 using namespace dvl;
@@ -281,43 +327,13 @@ dvl_status dvl_trim_head(const dvl_head *full, const int32_t *ranks, int32_t n_r
                          void *w_trim, uint8_t *scales_trim, int32_t *d2t,
                          int32_t *n_duplicates, void *stream)
 {
-    dvl_status st = check_head(full);
-    if (st != DVL_OK)
-        return st;
-    if ((int64_t)full->N != full->V || full->d2t || full->id_base != 0)
-        return DVL_ERR_INVALID_ARG;
-    if (!ranks || n_ranks < 1 || !w_trim || !aligned(w_trim, 16) || !d2t || !aligned(d2t, 4))
-        return DVL_ERR_INVALID_ARG;
-    if (full->dtype == DVL_NVFP4 && (!scales_trim || !aligned(scales_trim, 16)))
-        return DVL_ERR_INVALID_ARG;
-    std::vector<unsigned char> seen((size_t)full->V, 0);
-    int32_t dup = 0;
-    for (int32_t i = 0; i < n_ranks; ++i) {
-        const int32_t r = ranks[i];
-        if (r < 0 || (int64_t)r >= full->V)
-            return DVL_ERR_OUT_OF_RANGE;
-        if (seen[(size_t)r])
-            ++dup;
-        seen[(size_t)r] = 1;
-    }
-    if (n_duplicates)
-        *n_duplicates = dup;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e =
-        cudaMemcpyAsync(d2t, ranks, (size_t)n_ranks * sizeof(int32_t), cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess)
-        return cuda_failed(e);
-    const int64_t K = full->K;
-    if (full->dtype == DVL_BF16) {
-        e = launch_trim_rows(static_cast<const unsigned char *>(full->w), K * 2,
-                             static_cast<unsigned char *>(w_trim), d2t, n_ranks, s);
-    } else {
-        e = launch_trim_rows(static_cast<const unsigned char *>(full->w), K / 2,
-                             static_cast<unsigned char *>(w_trim), d2t, n_ranks, s);
-        if (e == cudaSuccess)
-            e = launch_trim_rows(full->scales, K / 16, scales_trim, d2t, n_ranks, s);
-    }
-    return e == cudaSuccess ? DVL_OK : cuda_failed(e);
+    return gather_rows(full, ranks, n_ranks, 0, w_trim, scales_trim, d2t, n_duplicates, stream);
+}
+
+dvl_status dvl_learn_rows(const dvl_head *full, const int32_t *ids, int32_t n, int32_t row0,
+                          void *w_trim, uint8_t *scales_trim, int32_t *d2t, void *stream)
+{
+    return gather_rows(full, ids, n, row0, w_trim, scales_trim, d2t, nullptr, stream);
 }
 
 const char *dvl_last_error(void) { return cudaGetErrorString(t_last_error); }

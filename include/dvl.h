@@ -236,6 +236,32 @@ dvl_status dvl_trim_head(const dvl_head *full, const int32_t *ranks, int32_t n_r
                          void *w_trim, uint8_t *scales_trim, int32_t *d2t,
                          int32_t *n_duplicates, void *stream);
 
+/* Learn escaped ids into spare rows of a trimmed head while serving ("Masked
+ * MTP drafts", section "Update (November 2026)": a static trim can miss;
+ * the server learns the escaped ids into spare head rows).  For i < n:
+ *   W_trim[row0 + i] = W_full[ids[i]] (the row's bytes; NVFP4 codes and
+ *   scales), d2t[row0 + i] = ids[i],
+ * the same copy as dvl_trim_head, into rows row0 .. row0 + n - 1.  Allocate
+ * the trimmed buffers with room for the rows they may learn; a head of
+ * row0 + n rows over the same buffers then includes the learned ids.
+ *   full:   the full head: N == V, d2t == NULL, id_base == 0.
+ *   ids:    HOST int32 [n], each in [0, V), checked before anything is
+ *           enqueued (DVL_ERR_OUT_OF_RANGE).
+ *   n:      >= 1.   row0: >= 0, with row0 + n < 2^31.
+ *   w_trim, scales_trim (NVFP4; NULL for bf16), d2t: the trimmed head's
+ *           device buffers from their row 0 (not offset); the caller owns
+ *           them and sizes them for rows up to row0 + n (not checkable here).
+ * Ordering: rows and d2t entries are written by kernels on `stream`; later
+ * calls on that stream see them.  The first reducing call after the learn
+ * on that stream must not set DVL_HEAD_STATIC on the trimmed head (the flag
+ * lets a kernel read the head before the preceding kernel has finished);
+ * later calls may set it again.  The ids are copied from pageable memory;
+ * the call returns once they have been read.
+ * Errors: DVL_ERR_INVALID_ARG, DVL_ERR_OUT_OF_RANGE (nothing enqueued),
+ * DVL_ERR_CUDA. */
+dvl_status dvl_learn_rows(const dvl_head *full, const int32_t *ids, int32_t n, int32_t row0,
+                          void *w_trim, uint8_t *scales_trim, int32_t *d2t, void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* Host-only ranks builder (no GPU involved)                              */
 /* ---------------------------------------------------------------------- */

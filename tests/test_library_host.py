@@ -175,3 +175,22 @@ def test_score_shape_and_pointer_checks(dvl):
     assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 1, None, 4, 0x4000, None) == 1
     assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 1, 0x2002, 4, 0x4000, None) == 1
     assert L.dvl_score_ids(ctypes.byref(h), 0x3000, 1, 0x2000, 4, None, None) == 1
+
+
+def test_learn_checks_reject_before_any_launch(dvl):
+    from draft_vocab_lm_gb300._native import lib
+    L = lib()
+    h = _head()
+    ids = (ctypes.c_int32 * 3)(4, 100, 7)  # 100 is outside [0, V)
+    assert L.dvl_learn_rows(ctypes.byref(h), ids, 3, 10, 0x1000, None, 0x2000, None) == 2
+    ok = (ctypes.c_int32 * 2)(4, 7)
+    assert L.dvl_learn_rows(ctypes.byref(h), ok, 0, 10, 0x1000, None, 0x2000, None) == 1
+    assert L.dvl_learn_rows(ctypes.byref(h), ok, 2, -1, 0x1000, None, 0x2000, None) == 1
+    assert L.dvl_learn_rows(ctypes.byref(h), ok, 2, 0x7fffffff, 0x1000, None, 0x2000, None) == 1
+    assert L.dvl_learn_rows(ctypes.byref(h), None, 2, 0, 0x1000, None, 0x2000, None) == 1
+    assert L.dvl_learn_rows(ctypes.byref(h), ok, 2, 0, 0x1008, None, 0x2000, None) == 1
+    assert L.dvl_learn_rows(ctypes.byref(h), ok, 2, 0, 0x1000, None, 0x2002, None) == 1
+    sliced = _head(N=50)  # not a full head
+    assert L.dvl_learn_rows(ctypes.byref(sliced), ok, 2, 0, 0x1000, None, 0x2000, None) == 1
+    nv = _head(dtype=1, scales=None)  # NVFP4 without scales
+    assert L.dvl_learn_rows(ctypes.byref(nv), ok, 2, 0, 0x1000, None, 0x2000, None) == 1
