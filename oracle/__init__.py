@@ -81,6 +81,10 @@ def _load():
     lib.oracle_logits_nvfp4.argtypes = [p, p, ctypes.c_float, i64, i64, p, i64, p,
                                         ctypes.c_int]
     lib.oracle_logits_nvfp4.restype = ctypes.c_int
+    lib.oracle_logits_fp8.argtypes = [p, ctypes.c_float, i64, i64, p, i64, p, ctypes.c_int]
+    lib.oracle_logits_fp8.restype = ctypes.c_int
+    lib.oracle_score_ids_fp8.argtypes = [p, ctypes.c_float, i64, i64, i64, p, i64, p, i64, p]
+    lib.oracle_score_ids_fp8.restype = None
     lib.oracle_score_ids_bf16.argtypes = [p, i64, i64, i64, p, i64, p, i64, p]
     lib.oracle_score_ids_bf16.restype = None
     lib.oracle_score_ids_nvfp4.argtypes = [p, p, ctypes.c_float, i64, i64, i64, p, i64, p,
@@ -189,6 +193,34 @@ def score_ids_nvfp4(q: np.ndarray, scales: np.ndarray, g: float, h: np.ndarray,
     out = np.empty((M, c), dtype=np.float32)
     _load().oracle_score_ids_nvfp4(_ptr(q), _ptr(scales), float(g), N, K, int(id_base),
                                    _ptr(h), M, _ptr(ids), c, _ptr(out))
+    return out
+
+
+def logits_fp8(q: np.ndarray, g: float, h: np.ndarray, nthreads: int = 0):
+    """fp32 logits of an FP8 head: q uint8[N][K] (E4M3 codes), g the fp32
+    tensor scale, h bf16 bits[M][K].  Returns (logits, threads)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    N, K = q.shape
+    M = h.shape[0]
+    assert h.shape[1] == K
+    out = np.empty((M, N), dtype=np.float32)
+    t = _load().oracle_logits_fp8(_ptr(q), float(g), N, K, _ptr(h), M, _ptr(out), nthreads)
+    return out, int(t)
+
+
+def score_ids_fp8(q: np.ndarray, g: float, h: np.ndarray, ids: np.ndarray, id_base: int = 0):
+    """score_ids_bf16 for an FP8 head (the same weight decode as logits_fp8)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    N, K = q.shape
+    M = h.shape[0]
+    assert h.shape[1] == K and ids.ndim == 2 and ids.shape[0] == M
+    c = ids.shape[1]
+    out = np.empty((M, c), dtype=np.float32)
+    _load().oracle_score_ids_fp8(_ptr(q), float(g), N, K, int(id_base), _ptr(h), M, _ptr(ids),
+                                 c, _ptr(out))
     return out
 
 

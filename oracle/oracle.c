@@ -32,6 +32,13 @@
  *       ids[m][j] - id_base, NaN for an id outside the head's rows ("Masked
  *       MTP drafts", section "Update (November 2026)": a drafter's candidates
  *       scored through the target's own LM head, bf16 or NVFP4).
+ *   FP8 head: w = float(e4m3(q)) * g, one fp32 rounding for the tensor
+ *       scale g, then the same dot product ("[DGX Spark] Qwen3.8-Flash-Next
+ *       on two DGX Sparks", section "The costs: a 69% smaller KV pool and
+ *       FP8 GDN weights": weights read as FP8 E4M3 halve the bytes; "Masked
+ *       MTP drafts": a drafter shipping an FP8 head).  The layout (row-major
+ *       codes, one byte per weight, one fp32 tensor scale) is the reading
+ *       this project adopts.
  *   trim check: W_trim[i] == W_full[ranks[i]] byte for byte, d2t[i] ==
  *       ranks[i] ("Masked MTP drafts": a ranks list next to the model, the
  *       head weight trimmed at load).
@@ -119,7 +126,7 @@ float oracle_nvfp4_weight(const uint8_t *q, const uint8_t *scales, float g,
 /* ------------------------------------------------------------------ */
 
 typedef struct {
-    int kind; /* 0 = bf16, 1 = nvfp4 */
+    int kind; /* 0 = bf16, 1 = nvfp4, 2 = fp8 */
     const uint16_t *w_bf16;
     const uint8_t *q;
     const uint8_t *scales;
@@ -140,9 +147,16 @@ static float row_dot(const logit_job *j, int64_t n, const uint16_t *hm)
             float prod = oracle_bf16_to_f32(wn[k]) * oracle_bf16_to_f32(hm[k]);
             acc = acc + prod;
         }
-    } else {
+    } else if (j->kind == 1) {
         for (int64_t k = 0; k < j->K; ++k) {
             float w = oracle_nvfp4_weight(j->q, j->scales, j->g, j->K, n, k);
+            float prod = w * oracle_bf16_to_f32(hm[k]);
+            acc = acc + prod;
+        }
+    } else {
+        const uint8_t *qn = j->q + n * j->K;
+        for (int64_t k = 0; k < j->K; ++k) {
+            float w = oracle_e4m3(qn[k]) * j->g;
             float prod = w * oracle_bf16_to_f32(hm[k]);
             acc = acc + prod;
         }
@@ -234,6 +248,22 @@ int oracle_logits_nvfp4(const uint8_t *q, const uint8_t *scales, float g, int64_
     return run_logits(j, nthreads);
 }
 
+int oracle_logits_fp8(const uint8_t *q, float g, int64_t N, int64_t K, const uint16_t *h,
+                      int64_t M, float *logits, int nthreads)
+{
+    logit_job j;
+    memset(&j, 0, sizeof j);
+    j.kind = 2;
+    j.q = q;
+    j.g = g;
+    j.N = N;
+    j.K = K;
+    j.M = M;
+    j.h = h;
+    j.logits = logits;
+    return run_logits(j, nthreads);
+}
+
 /* ------------------------------------------------------------------ */
 /* Candidate scores: the dot of the head row each id names.            */
 /* ------------------------------------------------------------------ */
@@ -274,6 +304,22 @@ void oracle_score_ids_nvfp4(const uint8_t *q, const uint8_t *scales, float g, in
     j.kind = 1;
     j.q = q;
     j.scales = scales;
+    j.g = g;
+    j.N = N;
+    j.K = K;
+    j.M = M;
+    j.h = h;
+    score_ids(&j, id_base, ids, c, out);
+}
+
+void oracle_score_ids_fp8(const uint8_t *q, float g, int64_t N, int64_t K, int64_t id_base,
+                          const uint16_t *h, int64_t M, const int32_t *ids, int64_t c,
+                          float *out)
+{
+    logit_job j;
+    memset(&j, 0, sizeof j);
+    j.kind = 2;
+    j.q = q;
     j.g = g;
     j.N = N;
     j.K = K;

@@ -24,6 +24,11 @@ int oracle_logits_bf16(const uint16_t *w, int64_t N, int64_t K, const uint16_t *
 int oracle_logits_nvfp4(const uint8_t *q, const uint8_t *scales, float g, int64_t N,
                         int64_t K, const uint16_t *h, int64_t M, float *logits,
                         int nthreads);
+int oracle_logits_fp8(const uint8_t *q, float g, int64_t N, int64_t K, const uint16_t *h,
+                      int64_t M, float *logits, int nthreads);
+void oracle_score_ids_fp8(const uint8_t *q, float g, int64_t N, int64_t K, int64_t id_base,
+                          const uint16_t *h, int64_t M, const int32_t *ids, int64_t c,
+                          float *out);
 void oracle_score_ids_bf16(const uint16_t *w, int64_t N, int64_t K, int64_t id_base,
                            const uint16_t *h, int64_t M, const int32_t *ids, int64_t c,
                            float *out);

@@ -56,7 +56,7 @@ def _e4m3_encode(x: np.ndarray):
     """Non-negative float64 -> (E4M3 byte, its value), round-to-nearest-even,
     saturating at 448; 2^-9 is the smallest subnormal."""
     x = np.clip(np.asarray(x, dtype=np.float64), 0.0, 448.0)
-    _, p = np.frexp(np.where(x > 0, x, 1.0))
+    _, p = np.frexp(np.where(x > 0, x, 2.0 ** -10))  # zero takes the subnormal path: byte 0
     e = np.maximum(p - 1, -6)              # binade exponent, floor at the subnormal one
     spacing = np.ldexp(1.0, e - 3)         # 3 mantissa bits
     units = np.rint(x / spacing)           # ties to even
@@ -105,6 +105,19 @@ def quantize_nvfp4(wbits: np.ndarray):
     return q, s_byte.reshape(N, K // 16), float(g)
 
 
+def quantize_fp8(wbits: np.ndarray, g: float | None = None):
+    """Quantize a bf16 head [N][K] to FP8 E4M3 with one fp32 tensor scale:
+    g = amax / 448 unless given; q = e4m3(|w| / g) with the sign in bit 7,
+    nearest-even, saturating at 448.  Returns (q uint8[N][K], g)."""
+    w = bf16_bits_to_f32(wbits).astype(np.float64)
+    if g is None:
+        amax = float(np.max(np.abs(w))) if w.size else 0.0
+        g = float(np.float32(amax / 448.0)) if amax > 0 else 1.0
+    byte, _ = _e4m3_encode(np.abs(w) / float(g))
+    q = np.where(w < 0, byte | np.uint8(0x80), byte).astype(np.uint8)
+    return q, float(g)
+
+
 # ---------------------------------------------------------------------------
 # Random tensors
 # ---------------------------------------------------------------------------
@@ -138,6 +151,31 @@ def normal_bf16_rows(seed: int, rows: int, K: int, std: float, tag: int = 0,
         with _cf.ThreadPoolExecutor(threads) as ex:
             list(ex.map(work, range(nblk)))
     return out
+
+
+def normal_fp8_rows(seed: int, rows: int, K: int, std: float, tag: int = 0,
+                    threads: int | None = None):
+    """An FP8 head: the rows of normal_bf16_rows(seed, rows, K, std, tag),
+    quantized block by block with the fixed tensor scale g = 6 std / 448 (so
+    no pass over the whole head is needed; |w| > 6 std saturates).
+    Returns (q uint8[rows][K], g)."""
+    g = float(np.float32(6.0 * std / 448.0))
+    out = np.empty((rows, K), dtype=np.uint8)
+    nblk = (rows + BLOCK_ROWS - 1) // BLOCK_ROWS
+
+    def work(b):
+        r0 = b * BLOCK_ROWS
+        r1 = min(rows, r0 + BLOCK_ROWS)
+        out[r0:r1] = quantize_fp8(_block_normals(seed, tag, b, r1 - r0, K, std), g)[0]
+
+    threads = threads or min(16, os.cpu_count() or 1)
+    if nblk <= 1 or threads <= 1:
+        for b in range(nblk):
+            work(b)
+    else:
+        with _cf.ThreadPoolExecutor(threads) as ex:
+            list(ex.map(work, range(nblk)))
+    return out, g
 
 
 def hidden_bf16(seed: int, M: int, K: int) -> np.ndarray:
