@@ -26,6 +26,7 @@ import subprocess
 import sys
 import threading
 import time
+import types
 
 import numpy as np
 
@@ -52,7 +53,8 @@ def parse():
     p.add_argument("--profile", nargs="?", const="c2m1", default=None,
                    help="only warm-up + timed calls of one workload, for ncu captures: "
                         "c2m1 (default), c2m3, c1m1, c1m3, c3m1, c4m8, c4m16, c4m32, c5m1, c5m3, "
-                        "scm16 (candidate scores, 16 rows x 32 through the c2 head)")
+                        "scm16 (candidate scores, 16 rows x 32 through the c2 head), "
+                        "f8m1, f8m3 (FP8 full-vocabulary head)")
     return p.parse_args()
 
 
@@ -294,6 +296,12 @@ def run_profile(args):
         wl = S.c5(Ms=(M,))
         head = dvl.Head(dev(torch, wl.q), scales=dev(torch, wl.scales), global_scale=wl.g,
                         V=wl.V, d2t=dev(torch, wl.d2t), static=True)
+    elif cfg == "f8":
+        # FP8 full-vocabulary head (the c2 rows quantized), M hidden rows
+        q8, g8 = S.normal_fp8_rows(1, S.V_FULL, 2560, 0.02)
+        head = dvl.Head(dev(torch, q8), fmt="fp8", global_scale=g8, V=S.V_FULL, static=True)
+        # the c2 hidden rows (the same seeds as the benchmark's)
+        wl = types.SimpleNamespace(h={M: S.hidden_bf16(1 + 100 * M, M, 2560)})
     elif cfg == "sc":
         # candidate scores through the full c2 head: M hidden rows x 32
         wl = S.c2(Ms=())
@@ -588,6 +596,19 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
         out[f"c5_nvfp4_32k_K5120_M{M}_argmax"] = entry(
             RL.call_bytes(wl5.N, wl5.K, M, dtype="nvfp4"), *t, peak, {"l2_rotation_copies": R5})
     del hs
+    # FP8 (E4M3, one tensor scale) full-vocabulary head, 248,320 x 2,560:
+    # the same rows as c2 at half the bytes
+    q8, g8 = S.normal_fp8_rows(1, N2, K2, 0.02)
+    head8 = dvl.Head(dev(torch, q8), fmt="fp8", global_scale=g8, V=N2, static=True)
+    del q8
+    for M, hh in ((1, h1), (3, h3)):
+        t = repeat_stats(torch, lambda i: dvl.draft_argmax(head8, hh, ids=ids, logits=lg, ws=ws),
+                         n_calls, R)
+        out[f"fp8_full_M{M}_argmax"] = entry(RL.call_bytes(N2, K2, M, dtype="fp8"), *t, peak)
+    t = repeat_stats(torch, lambda i: dvl.draft_topk(head8, h1, 4, ids=ids, logits=lg, ws=ws),
+                     n_calls, R)
+    out["fp8_full_M1_top4"] = entry(RL.call_bytes(N2, K2, 1, dtype="fp8", k=4), *t, peak)
+    del head8
     # trim vs full at M = 1 (same run)
     full = out["c2_full_M1_argmax"]["us_per_call"]
     out["trim_vs_full"] = {

@@ -23,7 +23,7 @@ import ctypes
 import numpy as np
 
 from . import roofline
-from ._native import (DVL_BF16, DVL_HEAD_STATIC, DVL_K_MULTIPLE, DVL_MAX_K, DVL_MAX_M,
+from ._native import (DVL_BF16, DVL_FP8, DVL_HEAD_STATIC, DVL_K_MULTIPLE, DVL_MAX_K, DVL_MAX_M,
                       DVL_MAX_TOPK, DVL_NVFP4, DvlError, DvlHead, check, lib)
 
 __all__ = [
@@ -53,13 +53,16 @@ def version() -> int:
 class Head:
     """A draft head resident on one CUDA device.
 
-    w:        bf16 [N][K] (any 2-byte dtype holding bfloat16 bits), or for
-              NVFP4 uint8 codes [N][K/2] (two E2M1 per byte, low nibble = even k).
+    w:        bf16 [N][K] (any 2-byte dtype holding bfloat16 bits); for
+              NVFP4 uint8 codes [N][K/2] (two E2M1 per byte, low nibble = even
+              k); for FP8 uint8 E4M3 codes [N][K] (with fmt="fp8").
     V:        full vocabulary size (ids lie in [0, V)); defaults to N.
     d2t:      int32 [N] full-vocabulary id of each row, or None (identity,
               shifted by id_base).
     scales:   NVFP4 only: uint8 E4M3 [N][K/16].
-    global_scale: NVFP4 tensor scale.
+    global_scale: NVFP4 / FP8 tensor scale.
+    fmt:      "bf16", "nvfp4" or "fp8"; by default NVFP4 when scales are
+              given, else bf16.
     static:   promise that no work still pending on the stream writes w,
               scales or d2t when a call is enqueued (weights loaded earlier;
               not a head trim_head has just filled on the same stream).  The
@@ -68,11 +71,23 @@ class Head:
     """
 
     def __init__(self, w, *, V: int | None = None, d2t=None, scales=None,
-                 global_scale: float = 1.0, id_base: int = 0, static: bool = False):
+                 global_scale: float = 1.0, id_base: int = 0, static: bool = False,
+                 fmt: str | None = None):
         torch = _torch()
         if not w.is_cuda or w.dim() != 2 or not w.is_contiguous():
             raise ValueError("w must be a contiguous 2-D CUDA tensor")
-        if scales is not None:
+        fmt = fmt or ("nvfp4" if scales is not None else "bf16")
+        if fmt not in ("bf16", "nvfp4", "fp8"):
+            raise ValueError("fmt must be bf16, nvfp4 or fp8")
+        if (fmt == "nvfp4") != (scales is not None):
+            raise ValueError("scales go with, and only with, an NVFP4 head")
+        self.fmt = fmt
+        if fmt == "fp8":
+            if w.element_size() != 1:
+                raise ValueError("FP8 codes must be a uint8 tensor")
+            self.dtype = DVL_FP8
+            self.K = w.shape[1]
+        elif scales is not None:
             if w.element_size() != 1:
                 raise ValueError("NVFP4 codes must be a uint8 tensor")
             self.dtype = DVL_NVFP4
@@ -216,16 +231,17 @@ def score_ids(head: Head, h, ids, *, logits=None, stream=None):
     return logits
 
 
-def trim_head(w_full, ranks, *, scales=None, stream=None):
+def trim_head(w_full, ranks, *, scales=None, fmt=None, stream=None):
     """Gather the rows `ranks` names (in its order) from a full head.
 
-    w_full: CUDA bf16 [V][K] or NVFP4 codes [V][K/2] (then `scales` [V][K/16]).
+    w_full: CUDA bf16 [V][K], NVFP4 codes [V][K/2] (then `scales` [V][K/16])
+            or FP8 codes [V][K] (fmt="fp8").
     ranks:  host ids (list, NumPy or CPU tensor).
     Returns (w_trim, scales_trim or None, d2t int32 CUDA [n], n_duplicates)."""
     torch = _torch()
     r = np.ascontiguousarray(np.asarray(ranks, dtype=np.int32))
     n = r.shape[0]
-    full = Head(w_full, scales=scales)
+    full = Head(w_full, scales=scales, fmt=fmt)
     w_trim = torch.empty((n, w_full.shape[1]), dtype=w_full.dtype, device=w_full.device)
     s_trim = None
     if scales is not None:
@@ -242,13 +258,13 @@ def trim_head(w_full, ranks, *, scales=None, stream=None):
 
 
 def learn_rows(w_full, ids, w_trim, d2t, row0: int, *, scales=None, scales_trim=None,
-               stream=None) -> None:
+               fmt=None, stream=None) -> None:
     """Copy the full head's rows `ids` (host ids) into rows row0 .. row0 + n - 1
     of trimmed buffers and set their d2t entries (dvl_learn_rows).  The first
     call on the stream afterwards must not treat the trimmed head as static;
     Shortlist takes care of that."""
     r = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
-    full = Head(w_full, scales=scales)
+    full = Head(w_full, scales=scales, fmt=fmt)
     check("dvl_learn_rows",
           lib().dvl_learn_rows(ctypes.byref(full.struct()), r.ctypes.data, r.shape[0], int(row0),
                                w_trim.data_ptr(),
@@ -271,7 +287,7 @@ class Shortlist:
     """
 
     def __init__(self, w_full, ranks, capacity: int, *, scales=None, global_scale: float = 1.0,
-                 stream=None):
+                 fmt=None, stream=None):
         torch = _torch()
         r = np.ascontiguousarray(np.asarray(ranks, dtype=np.int32))
         if capacity < r.shape[0]:
@@ -279,6 +295,7 @@ class Shortlist:
         self.V = w_full.shape[0]
         self.capacity = int(capacity)
         self.w_full, self.scales_full = w_full, scales
+        self.fmt = fmt or ("nvfp4" if scales is not None else "bf16")
         self.global_scale = float(global_scale)
         self.stream = stream
         self.w = torch.empty((capacity, w_full.shape[1]), dtype=w_full.dtype, device=w_full.device)
@@ -294,7 +311,7 @@ class Shortlist:
 
     def _append(self, ids: np.ndarray) -> None:
         learn_rows(self.w_full, ids, self.w, self.d2t, self.n, scales=self.scales_full,
-                   scales_trim=self.scales, stream=self.stream)
+                   scales_trim=self.scales, fmt=self.fmt, stream=self.stream)
         fresh = self.row_of[ids] < 0
         self.row_of[ids[fresh]] = self.n + np.nonzero(fresh)[0]
         self.n += ids.shape[0]
@@ -319,7 +336,8 @@ class Shortlist:
         kernels); later ones are, unless static=False."""
         hd = Head(self.w[:self.n], V=self.V, d2t=self.d2t[:self.n],
                   scales=self.scales[:self.n] if self.scales is not None else None,
-                  global_scale=self.global_scale, static=static and not self._pending)
+                  global_scale=self.global_scale, static=static and not self._pending,
+                  fmt=self.fmt)
         self._pending = False
         return hd
 

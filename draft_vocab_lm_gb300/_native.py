@@ -13,6 +13,7 @@ LIB_PATH = os.path.join(_HERE, "libdvl.so")
 
 DVL_BF16 = 0
 DVL_NVFP4 = 1
+DVL_FP8 = 2
 DVL_MAX_M = 32
 DVL_MAX_TOPK = 4
 DVL_K_MULTIPLE = 64

@@ -1,10 +1,16 @@
-// Fused projection + argmax / top-k over an NVFP4 draft head.  ("Masked MTP
-// drafts": requantizing the trimmed head to NVFP4 costs no measured
-// acceptance; the head read shrinks a further 3.6x against bf16.)
+// Fused projection + argmax / top-k over a low-bit draft head: NVFP4 or FP8.
+// ("Masked MTP drafts": requantizing the trimmed head to NVFP4 costs no
+// measured acceptance, and the head read shrinks a further 3.6x against
+// bf16; a drafter ships its own FP8 head.  "[DGX Spark] Qwen3.8-Flash-Next
+// on two DGX Sparks", section "The costs: a 69% smaller KV pool and FP8 GDN
+// weights": weights read as FP8 E4M3 halve the bytes.)
 //
-// Format read here: codes [N][K/2], two E2M1 values per byte with the even k
-// in the low nibble; scales [N][K/16], one E4M3 per 16 consecutive k of a
-// row; one fp32 tensor scale g.  weight = e2m1 * e4m3 * g.
+// Formats read here (FMT):
+//   NVFP4: codes [N][K/2], two E2M1 values per byte with the even k in the
+//          low nibble; scales [N][K/16], one E4M3 per 16 consecutive k of a
+//          row; one fp32 tensor scale g.  weight = e2m1 * e4m3 * g.
+//   FP8:   codes [N][K], one E4M3 per byte; one fp32 tensor scale g.
+//          weight = e4m3 * g.
 //
 // Decoding on CUDA cores costs more instructions per weight than HBM leaves
 // time for, so the products run on the tensor cores through the register
@@ -12,16 +18,18 @@
 // A operand straight from the registers the codes were decoded into:
 //   - the grid is persistent (two blocks per SM) and every warp owns one
 //     balanced contiguous range of head rows, walked as 16-row MMA tiles
-//     (the last one partial); lane (g, q) reads 16 bytes of codes (32
-//     weights, two scale blocks) of rows g and g + 8 per 128-wide k chunk,
-//     so a quad reads 64 contiguous bytes of each row;
+//     (the last one partial); lane (g, q) covers weights 32 q .. 32 q + 31
+//     of rows g and g + 8 in every 128-wide k chunk: 16 bytes of NVFP4 codes
+//     (two scale blocks) or 32 bytes of FP8 codes per row, so a quad reads
+//     one contiguous piece of each row;
 //   - a head the caller marked static starts filling the load ring before
 //     the wait for the preceding kernel; for the unrolled widths h is read
 //     from L2 once (its maximum and its staging from the same registers);
-//   - each code byte becomes an f16 pair with the exact E2M1x2 -> f16x2
-//     conversion and is multiplied by its block's E4M3 scale (E4M3x2 ->
+//   - NVFP4: each code byte becomes an f16 pair with the exact E2M1x2 ->
+//     f16x2 conversion and is multiplied by its block's E4M3 scale (E4M3x2 ->
 //     f16x2); the product has at most 6 significant bits and lies in
-//     [2^-10, 2688], so it is exact in f16;
+//     [2^-10, 2688], so it is exact in f16.  FP8: each pair of code bytes
+//     becomes an f16 pair with the exact E4M3x2 -> f16x2 conversion;
 //   - the hidden rows are staged once per block as f16 after an exact
 //     power-of-two rescale that puts their largest magnitude in [2^14, 2^15)
 //     (bf16 values within 2^31 of that maximum convert exactly; smaller ones
@@ -39,13 +47,19 @@
 #include "dvl_device.cuh"
 
 namespace dvl {
-namespace nvfp4 {
+namespace lowbit {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRows = 16;      // head rows per warp group (MMA M)
-constexpr int kChunk = 128;    // weights per row per k chunk (64 bytes of codes)
-constexpr int kNB = 4;         // k chunks of loads in flight per lane
+constexpr int kChunk = 128;    // weights per row per k chunk
+constexpr int kFmtNvfp4 = 0, kFmtFp8 = 1;
+// 16-byte code loads per row per chunk per lane, code bytes per row per
+// k chunk, and k chunks of loads in flight per lane (the same ~4.5 KB per
+// warp for both formats)
+template <int FMT> __host__ __device__ constexpr int q_words() { return FMT == kFmtFp8 ? 2 : 1; }
+template <int FMT> __host__ __device__ constexpr int chunk_bytes() { return FMT == kFmtFp8 ? 128 : 64; }
+template <int FMT> __host__ __device__ constexpr int ring_depth() { return FMT == kFmtFp8 ? 2 : 4; }
 constexpr int kLists = kWarps * 8;  // candidate lists per hidden row (8 row pairs per warp)
 
 // Four bytes of codes -> four f16x2 (byte t: low nibble in the low half).
@@ -69,6 +83,18 @@ __device__ __forceinline__ void e4m3_pair(uint32_t s16, uint32_t &lo2, uint32_t 
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(p) : "h"(s));
     lo2 = __byte_perm(p, p, 0x1010);
     hi2 = __byte_perm(p, p, 0x3232);
+}
+
+// Four bytes of E4M3 codes -> two f16x2 (bytes 0, 1 and 2, 3; the lower
+// byte in the low half).
+__device__ __forceinline__ void e4m3_word(uint32_t w, uint32_t &f0, uint32_t &f1)
+{
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(f0), "=r"(f1)
+        : "r"(w));
 }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
@@ -96,24 +122,26 @@ __device__ __forceinline__ float pow2f(int e)  // 2^e for e in [-126, 127], exac
 // [chunk][u][g][q] with g < M (unit = h[g][128 chunk + 32 q + 8 u .. +8]), so
 // that the reading lanes' units for one u are contiguous.  Lanes whose MMA
 // column g is M or more feed zeros and read nothing.
-__host__ __device__ inline size_t nvfp4_h_bytes(int Kpad, int M) { return (size_t)Kpad * 2 * M; }
+__host__ __device__ inline size_t lowbit_h_bytes(int Kpad, int M) { return (size_t)Kpad * 2 * M; }
 
 // K == KC (a multiple of 128) when KC > 0; K read from the arguments when 0.
-template <int M, int KM, int KC>
-__global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxArgs a)
+template <int FMT, int M, int KM, int KC>
+__global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const ArgmaxArgs a)
 {
+    constexpr int kNB = ring_depth<FMT>(), kQW = q_words<FMT>();
+    constexpr bool kNv = FMT == kFmtNvfp4;
     extern __shared__ __align__(16) unsigned char smem[];
     const int K = KC > 0 ? KC : a.K;
     const int Kpad = KC > 0 ? KC : a.Kpad, C = Kpad / kChunk;
     uint4 *s_h = reinterpret_cast<uint4 *>(smem);
-    uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + nvfp4_h_bytes(Kpad, M));
+    uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + lowbit_h_bytes(Kpad, M));
     __shared__ unsigned int s_wmax[kWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, q = lane & 3;
     const uint8_t *__restrict__ Q = static_cast<const uint8_t *>(a.w);
     const uint8_t *__restrict__ S = a.scales;
-    const size_t qrow = (size_t)K / 2, srow = (size_t)K / 16;
+    const size_t qrow = kNv ? (size_t)K / 2 : (size_t)K, srow = (size_t)K / 16;
 
     pdl_launch_dependents();
 
@@ -125,32 +153,42 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
     const int rend = (int)((long long)a.N * (gw + 1) / GW);
     const int my_groups = (rend - row0 + kRows - 1) / kRows;
 
-    // The load ring: codes (16 bytes) and scales (two E4M3) of rows ra / rb.
-    uint4 bqa[kNB], bqb[kNB];
+    // The load ring: codes (16 or 32 bytes) and, for NVFP4, scales (two
+    // E4M3) of rows ra / rb.
+    uint4 bqa[kNB][kQW], bqb[kNB][kQW];
     uint32_t bsa[kNB], bsb[kNB];
 #pragma unroll
     for (int b2 = 0; b2 < kNB; ++b2) {
-        bqa[b2] = bqb[b2] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int w = 0; w < kQW; ++w)
+            bqa[b2][w] = bqb[b2][w] = make_uint4(0u, 0u, 0u, 0u);
         bsa[b2] = bsb[b2] = 0u;
     }
     // compile-time K: a group's lane bases, codes of rows ra / rb at byte
-    // 16 q, scales at 2 q; loads are immediate offsets from them
-    constexpr int QR = KC / 2, SR = KC / 16;  // bytes per row: codes, scales
+    // 16 q (NVFP4) or 32 q (FP8), scales at 2 q; loads are immediate offsets
+    constexpr int QR = kNv ? KC / 2 : KC, SR = KC / 16;  // bytes per row: codes, scales
+    constexpr int CB = chunk_bytes<FMT>();
     auto bases = [&](int li, const uint8_t *&pqa, const uint8_t *&psa, bool &va, bool &vb) {
         const int ra = row0 + li * kRows + g;
         va = li < my_groups && ra < rend;
         vb = li < my_groups && ra + 8 < rend;
-        pqa = Q + (size_t)ra * QR + 16 * q;
+        pqa = Q + (size_t)ra * QR + 16 * kQW * q;
         psa = S + (size_t)ra * SR + 2 * q;
     };
     auto load = [&](int b2, const uint8_t *pqa, const uint8_t *psa, bool va, bool vb, int c) {
         if (va) {
-            bqa[b2] = ld_stream16(pqa + 64 * c);
-            bsa[b2] = __ldg(reinterpret_cast<const unsigned short *>(psa + 8 * c));
+#pragma unroll
+            for (int w = 0; w < kQW; ++w)
+                bqa[b2][w] = ld_stream16(pqa + CB * c + 16 * w);
+            if constexpr (kNv)
+                bsa[b2] = __ldg(reinterpret_cast<const unsigned short *>(psa + 8 * c));
         }
         if (vb) {
-            bqb[b2] = ld_stream16(pqa + 8 * QR + 64 * c);
-            bsb[b2] = __ldg(reinterpret_cast<const unsigned short *>(psa + 8 * SR + 8 * c));
+#pragma unroll
+            for (int w = 0; w < kQW; ++w)
+                bqb[b2][w] = ld_stream16(pqa + 8 * QR + CB * c + 16 * w);
+            if constexpr (kNv)
+                bsb[b2] = __ldg(reinterpret_cast<const unsigned short *>(psa + 8 * SR + 8 * c));
         }
     };
     const uint8_t *pqa = Q, *psa = S;
@@ -285,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
         hw[j] = 0u;
 
     // One 128-wide k chunk of rows ra (codes qa, scales sa) and rb.
-    auto chunk = [&](const uint4 &qa, const uint4 &qb, uint32_t sa, uint32_t sb, int cidx) {
+    auto chunk = [&](const uint4 (&qa)[kQW], const uint4 (&qb)[kQW], uint32_t sa, uint32_t sb,
+                     int cidx) {
         if (g < M) {
             const uint4 *hp = s_h + (size_t)cidx * (16 * M) + (g * 4 + q);
 #pragma unroll
@@ -294,26 +333,48 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
                 hw[4 * u] = v.x; hw[4 * u + 1] = v.y; hw[4 * u + 2] = v.z; hw[4 * u + 3] = v.w;
             }
         }
-        uint32_t sa_lo, sa_hi, sb_lo, sb_hi;
-        e4m3_pair(sa, sa_lo, sa_hi);
-        e4m3_pair(sb, sb_lo, sb_hi);
+        if constexpr (!kNv) {
+            // FP8: code word t (k = 32 q + 4 t .. + 3) of each row is exactly
+            // the A operand of MMA t: decode it as it is used
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const uint4 &xa = qa[t >> 2], &xb = qb[t >> 2];
+                const uint32_t wa = (t & 3) == 0 ? xa.x : (t & 3) == 1 ? xa.y : (t & 3) == 2 ? xa.z : xa.w;
+                const uint32_t wb = (t & 3) == 0 ? xb.x : (t & 3) == 1 ? xb.y : (t & 3) == 2 ? xb.z : xb.w;
+                uint32_t a0, a2, a1, a3;
+                e4m3_word(wa, a0, a2);
+                e4m3_word(wb, a1, a3);
+                mma_f16(acc[t & 3], a0, a1, a2, a3, hw[2 * t], hw[2 * t + 1]);
+            }
+            return;
+        }
+        // fa[i], fb[i]: the f16 pair of k = 32 q + 2 i, + 1 of rows ra, rb
         uint32_t fa[16], fb[16];
-        const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
-        const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+        if constexpr (kNv) {
+            uint32_t sa_lo, sa_hi, sb_lo, sb_hi;
+            e4m3_pair(sa, sa_lo, sa_hi);
+            e4m3_pair(sb, sb_lo, sb_hi);
+            const uint32_t wa[4] = {qa[0].x, qa[0].y, qa[0].z, qa[0].w};
+            const uint32_t wb[4] = {qb[0].x, qb[0].y, qb[0].z, qb[0].w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t t4[4];
-            e2m1_word(wa[j], t4);
-            fa[4 * j] = t4[0]; fa[4 * j + 1] = t4[1]; fa[4 * j + 2] = t4[2]; fa[4 * j + 3] = t4[3];
-            e2m1_word(wb[j], t4);
-            fb[4 * j] = t4[0]; fb[4 * j + 1] = t4[1]; fb[4 * j + 2] = t4[2]; fb[4 * j + 3] = t4[3];
+            for (int j = 0; j < 4; ++j) {
+                uint32_t t4[4];
+                e2m1_word(wa[j], t4);
+                fa[4 * j] = t4[0]; fa[4 * j + 1] = t4[1]; fa[4 * j + 2] = t4[2]; fa[4 * j + 3] = t4[3];
+                e2m1_word(wb[j], t4);
+                fb[4 * j] = t4[0]; fb[4 * j + 1] = t4[1]; fb[4 * j + 2] = t4[2]; fb[4 * j + 3] = t4[3];
+            }
+            // the block scale: k < 32 q + 16 uses the lower scale byte
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                fa[i] = hmul2(fa[i], i < 8 ? sa_lo : sa_hi);
+                fb[i] = hmul2(fb[i], i < 8 ? sb_lo : sb_hi);
+            }
         }
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const uint32_t sca = t < 4 ? sa_lo : sa_hi, scb = t < 4 ? sb_lo : sb_hi;
-            mma_f16(acc[t & 3], hmul2(fa[2 * t], sca), hmul2(fb[2 * t], scb),
-                    hmul2(fa[2 * t + 1], sca), hmul2(fb[2 * t + 1], scb), hw[2 * t], hw[2 * t + 1]);
-        }
+        for (int t = 0; t < 8; ++t)
+            mma_f16(acc[t & 3], fa[2 * t], fb[2 * t], fa[2 * t + 1], fb[2 * t + 1], hw[2 * t],
+                    hw[2 * t + 1]);
     };
     // Rows ra (c0, c1) and rb (c2, c3) of a finished group; hidden rows 2q, 2q + 1.
     auto finish_group = [&](int ra, int ida, int idb) {
@@ -345,13 +406,16 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
         // ---- compile-time K: one base pointer per group, immediate offsets ----
         constexpr int CC = KC / kChunk;
         static_assert(CC % kNB == 0, "the ring must divide the chunks");
+        // NVFP4 unrolls the whole group; FP8 (twice the code bytes per
+        // chunk) a multiple of the ring, which keeps it within the registers
+        constexpr int kCU = kNv ? CC : 2 * kNB;
         for (int li = 0; li < my_groups; ++li) {
             const uint8_t *nqa, *nsa;
             bool nva, nvb;
             bases(li + 1, nqa, nsa, nva, nvb);
             const int ra = row0 + li * kRows + g;
             const int ida = row_id(ra), idb = row_id(ra + 8);
-#pragma unroll
+#pragma unroll(kCU)
             for (int c = 0; c < CC; ++c) {
                 const int b2 = c % kNB;
                 chunk(bqa[b2], bqb[b2], bsa[b2], bsb[b2], c);
@@ -373,20 +437,28 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
         auto issue = [&](int b2) {
             const int ra = row0 + li * kRows + g, rb = ra + 8;
             const int kc = kChunk * lc + 32 * q;
-            const bool kin = li < my_groups && kc < K;
-            bqa[b2] = make_uint4(0u, 0u, 0u, 0u);
-            bqb[b2] = make_uint4(0u, 0u, 0u, 0u);
+            const bool kin = li < my_groups && kc < K;  // K % 64 == 0: all 32 k in range
+            const size_t cb = kNv ? (size_t)kc / 2 : (size_t)kc;  // code byte of k = kc
+#pragma unroll
+            for (int w = 0; w < kQW; ++w)
+                bqa[b2][w] = bqb[b2][w] = make_uint4(0u, 0u, 0u, 0u);
             bsa[b2] = 0u;
             bsb[b2] = 0u;
             if (kin && ra < rend) {
-                bqa[b2] = ld_stream16(Q + (size_t)ra * qrow + kc / 2);
-                bsa[b2] = __ldg(
-                    reinterpret_cast<const unsigned short *>(S + (size_t)ra * srow + kc / 16));
+#pragma unroll
+                for (int w = 0; w < kQW; ++w)
+                    bqa[b2][w] = ld_stream16(Q + (size_t)ra * qrow + cb + 16 * w);
+                if constexpr (kNv)
+                    bsa[b2] = __ldg(reinterpret_cast<const unsigned short *>(
+                        S + (size_t)ra * srow + kc / 16));
             }
             if (kin && rb < rend) {
-                bqb[b2] = ld_stream16(Q + (size_t)rb * qrow + kc / 2);
-                bsb[b2] = __ldg(
-                    reinterpret_cast<const unsigned short *>(S + (size_t)rb * srow + kc / 16));
+#pragma unroll
+                for (int w = 0; w < kQW; ++w)
+                    bqb[b2][w] = ld_stream16(Q + (size_t)rb * qrow + cb + 16 * w);
+                if constexpr (kNv)
+                    bsb[b2] = __ldg(reinterpret_cast<const unsigned short *>(
+                        S + (size_t)rb * srow + kc / 16));
             }
             if (++lc == C) {
                 lc = 0;
@@ -433,15 +505,15 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_nvfp4_kernel(const ArgmaxA
     block_finish<KM>(s_cand, M, kLists, a);
 }
 
-template <int M, int KM, int KC>
+template <int FMT, int M, int KM, int KC>
 cudaError_t launch_one(const ArgmaxArgs &a, cudaStream_t s)
 {
-    const size_t smem = nvfp4_h_bytes(a.Kpad, M) + (size_t)M * kLists * KM * 8;
+    const size_t smem = lowbit_h_bytes(a.Kpad, M) + (size_t)M * kLists * KM * 8;
     DeviceInfo di;
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess)
         return e;
-    auto kern = argmax_nvfp4_kernel<M, KM, KC>;
+    auto kern = argmax_lowbit_kernel<FMT, M, KM, KC>;
     int per_sm = 0;
     e = blocks_per_sm(reinterpret_cast<const void *>(kern), kThreads, smem, &per_sm);
     if (e != cudaSuccess)
@@ -467,21 +539,58 @@ cudaError_t launch_one(const ArgmaxArgs &a, cudaStream_t s)
 
 inline int kpad_of(int K) { return (K + kChunk - 1) / kChunk * kChunk; }
 
-template <int KM, int KC>
+template <int FMT, int KM, int KC>
 cudaError_t dispatch_m(const ArgmaxArgs &a, int M, cudaStream_t s)
 {
     switch (M) {
-    case 1: return launch_one<1, KM, KC>(a, s);
-    case 2: return launch_one<2, KM, KC>(a, s);
-    case 3: return launch_one<3, KM, KC>(a, s);
-    case 4: return launch_one<4, KM, KC>(a, s);
-    case 5: return launch_one<5, KM, KC>(a, s);
-    case 6: return launch_one<6, KM, KC>(a, s);
-    case 7: return launch_one<7, KM, KC>(a, s);
-    case 8: return launch_one<8, KM, KC>(a, s);
+    case 1: return launch_one<FMT, 1, KM, KC>(a, s);
+    case 2: return launch_one<FMT, 2, KM, KC>(a, s);
+    case 3: return launch_one<FMT, 3, KM, KC>(a, s);
+    case 4: return launch_one<FMT, 4, KM, KC>(a, s);
+    case 5: return launch_one<FMT, 5, KM, KC>(a, s);
+    case 6: return launch_one<FMT, 6, KM, KC>(a, s);
+    case 7: return launch_one<FMT, 7, KM, KC>(a, s);
+    case 8: return launch_one<FMT, 8, KM, KC>(a, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
-}  // namespace nvfp4
+// argmax at the unrolled widths (K = 2,560 or 5,120, M <= 4): one base
+// pointer per group with immediate offsets.
+template <int FMT>
+cudaError_t launch_kc(const ArgmaxArgs &a, int M, cudaStream_t s)
+{
+    if (a.K == 5120) {
+        switch (M) {
+        case 1: return launch_one<FMT, 1, 1, 5120>(a, s);
+        case 2: return launch_one<FMT, 2, 1, 5120>(a, s);
+        case 3: return launch_one<FMT, 3, 1, 5120>(a, s);
+        case 4: return launch_one<FMT, 4, 1, 5120>(a, s);
+        }
+    } else if (a.K == 2560) {
+        switch (M) {
+        case 1: return launch_one<FMT, 1, 1, 2560>(a, s);
+        case 2: return launch_one<FMT, 2, 1, 2560>(a, s);
+        case 3: return launch_one<FMT, 3, 1, 2560>(a, s);
+        case 4: return launch_one<FMT, 4, 1, 2560>(a, s);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+// argmax / top-k with K read at run time, M <= 8.
+template <int FMT>
+cudaError_t launch_rt(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s)
+{
+    return kmax == 1 ? dispatch_m<FMT, 1, 0>(a, M, s) : dispatch_m<FMT, 4, 0>(a, M, s);
+}
+
+// Each format's instantiations live in a translation unit of their own
+// (compiled in parallel).
+extern template cudaError_t launch_kc<kFmtNvfp4>(const ArgmaxArgs &, int, cudaStream_t);
+extern template cudaError_t launch_kc<kFmtFp8>(const ArgmaxArgs &, int, cudaStream_t);
+extern template cudaError_t launch_rt<kFmtNvfp4>(const ArgmaxArgs &, int, int, cudaStream_t);
+extern template cudaError_t launch_rt<kFmtFp8>(const ArgmaxArgs &, int, int, cudaStream_t);
+
+}  // namespace lowbit
 }  // namespace dvl

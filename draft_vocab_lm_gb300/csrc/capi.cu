@@ -107,7 +107,7 @@ dvl_status check_head(const dvl_head *hd)
 {
     if (!hd)
         return DVL_ERR_INVALID_ARG;
-    if (hd->dtype != DVL_BF16 && hd->dtype != DVL_NVFP4)
+    if (hd->dtype != DVL_BF16 && hd->dtype != DVL_NVFP4 && hd->dtype != DVL_FP8)
         return DVL_ERR_INVALID_ARG;
     if ((hd->flags & ~DVL_HEAD_STATIC) != 0 || hd->reserved2 != 0)
         return DVL_ERR_INVALID_ARG;
@@ -118,6 +118,8 @@ dvl_status check_head(const dvl_head *hd)
     if (!hd->w || !aligned(hd->w, 16))
         return DVL_ERR_INVALID_ARG;
     if (hd->dtype == DVL_NVFP4 && (!hd->scales || !aligned(hd->scales, 16)))
+        return DVL_ERR_INVALID_ARG;
+    if (hd->dtype != DVL_NVFP4 && hd->scales)
         return DVL_ERR_INVALID_ARG;
     if (hd->d2t) {
         if (!aligned(hd->d2t, 4))
@@ -141,7 +143,7 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
     if (!ws || !aligned(ws, 16) || ws_bytes < dvl_workspace_bytes(M, k))
         return DVL_ERR_WORKSPACE;
     const int chunk =
-        hd->dtype == DVL_BF16 ? max_chunk_rows_bf16(hd->K) : max_chunk_rows_nvfp4(hd->K);
+        hd->dtype == DVL_BF16 ? max_chunk_rows_bf16(hd->K) : max_chunk_rows_lowbit(hd->K);
     if (chunk < 1)
         return DVL_ERR_UNSUPPORTED;
     ArgmaxArgs a;
@@ -173,7 +175,7 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
         a.ids = ids + (size_t)m0 * k;
         a.logits = logits + (size_t)m0 * k;
         cudaError_t e = hd->dtype == DVL_BF16 ? launch_argmax_bf16(a, mc, kmax, s)
-                                              : launch_argmax_nvfp4(a, mc, kmax, s);
+                                              : launch_argmax_lowbit(a, hd->dtype, mc, kmax, s);
         if (e != cudaSuccess)
             return cuda_failed(e);
     }
@@ -231,7 +233,7 @@ static dvl_status gather_rows(const dvl_head *full, const int32_t *ids, int32_t 
     if (e != cudaSuccess)
         return cuda_failed(e);
     const int64_t K = full->K;
-    const int64_t wrow = full->dtype == DVL_BF16 ? K * 2 : K / 2;
+    const int64_t wrow = full->dtype == DVL_BF16 ? K * 2 : full->dtype == DVL_FP8 ? K : K / 2;
     e = launch_trim_rows(static_cast<const unsigned char *>(full->w), wrow,
                          static_cast<unsigned char *>(w_trim) + (int64_t)row0 * wrow, d2t_rows, n,
                          s);

@@ -20,9 +20,9 @@ constexpr size_t kWsSlots = 512;          // uint64[kMaxCtas][M][kmax] (k > 1)
 
 // Arguments of one reducing launch (one chunk of at most 8 hidden rows).
 struct ArgmaxArgs {
-    const void *w;            // bf16 [N][K] or NVFP4 codes [N][K/2]
+    const void *w;            // bf16 [N][K], NVFP4 codes [N][K/2] or FP8 codes [N][K]
     const uint8_t *scales;    // NVFP4 E4M3 [N][K/16]
-    float gscale;             // NVFP4 tensor scale
+    float gscale;             // NVFP4 / FP8 tensor scale
     const int32_t *d2t;       // int32 [N] or nullptr
     int64_t id_base;          // full id of row 0 when d2t is null
     int N, K, Kpad;           // Kpad: K rounded up to the kernel's k-step
@@ -50,12 +50,15 @@ cudaError_t blocks_per_sm(const void *func, int threads, size_t smem, int *out);
 // Launchers (return the launch's cudaError_t).  M is the chunk's row count
 // (1 .. 8), kmax is 1 (argmax) or 4 (top-k).
 cudaError_t launch_argmax_bf16(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
-cudaError_t launch_argmax_nvfp4(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
+// NVFP4 and FP8 heads (dtype DVL_NVFP4 or DVL_FP8), on the register-path
+// tensor cores.
+cudaError_t launch_argmax_lowbit(const ArgmaxArgs &a, int dtype, int M, int kmax,
+                                 cudaStream_t s);
 int max_chunk_rows_bf16(int K);
 // Tensor-core argmax (bf16, k = 1) for 9..32 hidden rows in one launch.
 bool tc_argmax_supported(int M, int K);
 cudaError_t launch_argmax_tc(const ArgmaxArgs &a, int M, cudaStream_t s);
-int max_chunk_rows_nvfp4(int K);
+int max_chunk_rows_lowbit(int K);
 
 // The argument checks of draft_argmax / draft_topk, without the workspace.
 dvl_status check_reduce_args(const dvl_head *hd, const void *h, int32_t M, int32_t k,
@@ -64,10 +67,10 @@ dvl_status check_reduce_args(const dvl_head *hd, const void *h, int32_t M, int32
 // Arguments of a candidate-scoring launch: out[m][j] = W[ids[m][j] - id_base]
 // . h[m] for m < M, j < c (NaN for an id outside the head's N rows).
 struct ScoreArgs {
-    int dtype;                // DVL_BF16 or DVL_NVFP4
-    const void *w;            // bf16 [N][K] or NVFP4 codes [N][K/2]
+    int dtype;                // DVL_BF16, DVL_NVFP4 or DVL_FP8
+    const void *w;            // bf16 [N][K], NVFP4 codes [N][K/2] or FP8 codes [N][K]
     const uint8_t *scales;    // NVFP4 E4M3 [N][K/16]
-    float gscale;             // NVFP4 tensor scale
+    float gscale;             // NVFP4 / FP8 tensor scale
     int64_t id_base;          // id of row 0
     int N, K, M, c;
     const uint16_t *h;        // bf16 [M][K]

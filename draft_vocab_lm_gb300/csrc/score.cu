@@ -2,7 +2,7 @@
 // the logit of the head row the candidate id names.  ("Masked MTP drafts",
 // section "Update (November 2026)": a drafter that carries no head of its
 // own scores its candidates through the target's LM head, bf16 or NVFP4,
-// and the trim stacks on top.)
+// and the trim stacks on top; FP8 heads are read the same way.)
 //
 // A gather-GEMV: the rows are scattered, few (M x c dots) and each is read
 // once, so the kernel is bound by memory latency, not bandwidth.  One warp
@@ -17,6 +17,9 @@
 //     exactly (E2M1x2 -> f16x2 -> fp32, E4M3 -> fp32), the block's products
 //     (exact in fp32) are summed and multiplied by the block scale, and the
 //     tensor scale is applied to the finished dot;
+//   - FP8: lane l covers 16 weights (one 16-byte load) of every 512-wide k
+//     step, decoded exactly (E4M3x2 -> f16x2 -> fp32), the tensor scale on
+//     the finished dot;
 //   - the lanes' partial sums meet in a butterfly; lane 0 writes the logit,
 //     or NaN when the id is outside the head's rows.
 #include <cuda_fp16.h>
@@ -170,6 +173,55 @@ __global__ void __launch_bounds__(kThreads) score_nvfp4_kernel(const ScoreArgs a
     }
 }
 
+// FP8: lane l covers 16 weights (16 code bytes, one load) of every 512-wide
+// k step; E4M3x2 -> f16x2 -> fp32 is exact and so is each product with h.
+__global__ void __launch_bounds__(kThreads) score_fp8_kernel(const ScoreArgs a)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const long long total = (long long)a.M * a.c;
+    const long long GW = (long long)gridDim.x * kWarps;
+    const uint8_t *__restrict__ Q = static_cast<const uint8_t *>(a.w);
+    const int K = a.K;
+    for (long long p = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5); p < total; p += GW) {
+        const int m = (int)(p / a.c);
+        const long long row = pair_row(a, p);
+        float acc = 0.f;
+        if (row >= 0) {
+            const uint8_t *qr = Q + row * K;
+            const uint16_t *hr = a.h + (size_t)m * K;
+#pragma unroll 2
+            for (int k0 = 16 * lane; k0 < K; k0 += 512) {
+                const uint4 codes = ld_stream16(qr + k0);
+                const uint4 h0 = __ldg(reinterpret_cast<const uint4 *>(hr + k0));
+                const uint4 h1 = __ldg(reinterpret_cast<const uint4 *>(hr + k0 + 8));
+                const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+                const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t f0, f1;
+                    asm("{\n\t.reg .b16 lo, hi;\n\t"
+                        "mov.b32 {lo, hi}, %2;\n\t"
+                        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+                        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+                        : "=r"(f0), "=r"(f1)
+                        : "r"(cw[i]));
+                    const float2 w0 = __half22float2(*reinterpret_cast<const __half2 *>(&f0));
+                    const float2 w1 = __half22float2(*reinterpret_cast<const __half2 *>(&f1));
+                    acc = fmaf(w0.x, bf16_lo(hw[2 * i]), acc);
+                    acc = fmaf(w0.y, bf16_hi(hw[2 * i]), acc);
+                    acc = fmaf(w1.x, bf16_lo(hw[2 * i + 1]), acc);
+                    acc = fmaf(w1.y, bf16_hi(hw[2 * i + 1]), acc);
+                }
+            }
+        }
+        acc = warp_sum(acc) * a.gscale;
+        if (lane == 0)
+            a.out[p] = row >= 0 ? acc : __int_as_float(0x7fc00000);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_score(const ScoreArgs &a, cudaStream_t s)
@@ -187,6 +239,8 @@ cudaError_t launch_score(const ScoreArgs &a, cudaStream_t s)
         grid = 1;
     if (a.dtype == DVL_NVFP4)
         return launch_pdl(score_nvfp4_kernel, (unsigned)grid, kThreads, 0, s, a);
+    if (a.dtype == DVL_FP8)
+        return launch_pdl(score_fp8_kernel, (unsigned)grid, kThreads, 0, s, a);
     if (a.K == 2560)
         return launch_pdl(score_bf16_kernel<2560>, (unsigned)grid, kThreads, 0, s, a);
     if (a.K == 5120)

@@ -17,11 +17,14 @@ NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 
 def head_bytes(N: int, K: int, dtype: str = "bf16") -> int:
     """Bytes of an N x K head: bf16 2 B per weight; NVFP4 half a byte per
-    weight plus one E4M3 scale per 16 weights plus the fp32 tensor scale."""
+    weight plus one E4M3 scale per 16 weights plus the fp32 tensor scale;
+    FP8 one byte per weight plus the fp32 tensor scale."""
     if dtype == "bf16":
         return N * K * 2
     if dtype == "nvfp4":
         return N * K // 2 + N * K // 16 + 4
+    if dtype == "fp8":
+        return N * K + 4
     raise ValueError(dtype)
 
 
@@ -36,7 +39,7 @@ def score_bytes(M: int, c: int, K: int, dtype: str = "bf16") -> int:
     """Algorithmic bytes of one candidate-scoring call: each named head row
     (M*c rows, repeats counted once per candidate), the hidden rows, the ids
     and the fp32 scores."""
-    row = head_bytes(1, K, dtype) - (4 if dtype == "nvfp4" else 0)
+    row = head_bytes(1, K, dtype) - (0 if dtype == "bf16" else 4)
     return M * c * row + M * K * 2 + M * c * 8
 
 

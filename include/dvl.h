@@ -17,7 +17,10 @@
  *     next to the model, the head weight trimmed at load; EAGLE-3's d2t
  *     index mapping reused for a frequency-ranked subset);
  *   - the NVFP4 head ("Masked MTP drafts": the trimmed head requantized to
- *     NVFP4);
+ *     NVFP4) and the FP8 head ("Masked MTP drafts", section "Update
+ *     (November 2026)": a drafter's own FP8 head; "[DGX Spark]
+ *     Qwen3.8-Flash-Next on two DGX Sparks", section "The costs: a 69%
+ *     smaller KV pool and FP8 GDN weights": weights read as FP8 E4M3);
  *   - the ranks builder ("Shortlist MTP", section "Building the 16k
  *     shortlist"; "[DGX Spark] Qwen3.8-Flash-Next on two DGX Sparks",
  *     section "Build the draft vocabulary from your own text").
@@ -59,9 +62,11 @@ typedef enum {
 
 typedef enum {
     DVL_BF16 = 0,  /* W: bfloat16 [N][K] row-major                          */
-    DVL_NVFP4 = 1  /* W: E2M1 codes [N][K/2] (low nibble = even k), E4M3
+    DVL_NVFP4 = 1, /* W: E2M1 codes [N][K/2] (low nibble = even k), E4M3
                       scales [N][K/16] (one per 16 consecutive k of a row),
                       one fp32 tensor scale                                  */
+    DVL_FP8 = 2    /* W: E4M3 codes [N][K], one fp32 tensor scale; no
+                      per-block scales                                       */
 } dvl_dtype;
 
 /* Limits of this build. */
@@ -89,9 +94,9 @@ typedef struct dvl_head {
     int64_t id_base;      /* with d2t == NULL, row n has full id id_base + n;
                              id_base + N <= V.  0 for a whole head; the first
                              id of a slice when a head is split by rows.       */
-    const void *w;        /* bf16 [N][K], or NVFP4 codes [N][K/2]              */
-    const uint8_t *scales;/* NVFP4: E4M3 [N][K/16]; NULL for bf16              */
-    float global_scale;   /* NVFP4 tensor scale; ignored for bf16              */
+    const void *w;        /* bf16 [N][K], NVFP4 codes [N][K/2] or FP8 [N][K]   */
+    const uint8_t *scales;/* NVFP4: E4M3 [N][K/16]; NULL for bf16 and FP8      */
+    float global_scale;   /* NVFP4 / FP8 tensor scale; ignored for bf16        */
     int32_t reserved2;    /* must be 0                                         */
     const int32_t *d2t;   /* int32 [N]: full-vocabulary id of each row, each in
                              [0, V) (the kernels do not check); NULL means the
@@ -136,8 +141,9 @@ dvl_status dvl_workspace_init(void *ws, size_t bytes, void *stream);
  * id; a NaN logit ranks below every number (among NaN logits the lowest id
  * wins, reported with a NaN logit); -0 and +0 compare equal and +0 is
  * reported.  For NVFP4,
- * weight = e2m1(code) * e4m3(scale) * global_scale, and the kernel applies
- * global_scale to the finished dot product.
+ * weight = e2m1(code) * e4m3(scale) * global_scale; for FP8,
+ * weight = e4m3(code) * global_scale; the kernel applies global_scale to the
+ * finished dot product.
  *   head:      the head (see dvl_head); host struct, device pointers.
  *   h:         device bf16 [M][K], row-major.
  *   M:         1 .. DVL_MAX_M.
@@ -147,7 +153,8 @@ dvl_status dvl_workspace_init(void *ws, size_t bytes, void *stream);
  *              bytes, zeroed once by dvl_workspace_init.
  * Errors: DVL_ERR_INVALID_ARG (NULL, misaligned, N < 1, K not a multiple of
  * 64 or above DVL_MAX_K, M out of range, unknown flags, reserved2 non-zero, dtype
- * unknown, NVFP4 without scales, d2t == NULL with id_base + N > V),
+ * unknown, NVFP4 without scales, FP8 with scales, d2t == NULL with
+ * id_base + N > V),
  * DVL_ERR_WORKSPACE, DVL_ERR_CUDA. */
 dvl_status dvl_draft_argmax(const dvl_head *head, const void *h, int32_t M,
                             int32_t *ids, float *max_logit, void *ws,
@@ -196,7 +203,8 @@ dvl_status dvl_draft_argmax_noalloc(const dvl_head *head, const void *h, int32_t
  * stacks on top).  For m < M and j < c:
  *   logits[m][j] = sum_k W[ids[m][j] - id_base][k] * h[m][k]
  * with the head's dtype and arithmetic (fp32 accumulation; NVFP4 weights
- * e2m1 * e4m3 with the tensor scale on the finished dot), in any summation
+ * e2m1 * e4m3, FP8 weights e4m3, with the tensor scale on the finished dot),
+ * in any summation
  * order.  The head's rows are ids id_base .. id_base + N - 1: a full head
  * (id_base 0) or any contiguous slice of one.  An id outside them scores
  * NaN; the ids live on the device and are not checked on the host.
@@ -217,7 +225,7 @@ dvl_status dvl_score_ids(const dvl_head *head, const void *h, int32_t M,
 /* ---------------------------------------------------------------------- */
 
 /* Trim a full head to the rows a ranks list names, in the list's order:
- * W_trim[i] = W_full[ranks[i]] (byte copy of the row; for NVFP4 the codes
+ * W_trim[i] = W_full[ranks[i]] (byte copy of the row, in any dtype; for NVFP4 the codes
  * and the scales), d2t[i] = ranks[i].  The ranks are checked on the host
  * before anything is enqueued; duplicates are accepted (padded lists exist)
  * and counted.

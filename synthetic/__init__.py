@@ -109,13 +109,19 @@ def quantize_fp8(wbits: np.ndarray, g: float | None = None):
     """Quantize a bf16 head [N][K] to FP8 E4M3 with one fp32 tensor scale:
     g = amax / 448 unless given; q = e4m3(|w| / g) with the sign in bit 7,
     nearest-even, saturating at 448.  Returns (q uint8[N][K], g)."""
-    w = bf16_bits_to_f32(wbits).astype(np.float64)
+    wbits = np.asarray(wbits, dtype=np.uint16)
     if g is None:
-        amax = float(np.max(np.abs(w))) if w.size else 0.0
+        amax = float(np.max(np.abs(bf16_bits_to_f32(wbits)))) if wbits.size else 0.0
         g = float(np.float32(amax / 448.0)) if amax > 0 else 1.0
-    byte, _ = _e4m3_encode(np.abs(w) / float(g))
-    q = np.where(w < 0, byte | np.uint8(0x80), byte).astype(np.uint8)
-    return q, float(g)
+    # a bf16 weight has 65,536 possible bit patterns: encode each once
+    with np.errstate(invalid="ignore"):  # the signalling-NaN patterns
+        v = bf16_bits_to_f32(np.arange(65536, dtype=np.uint32).astype(np.uint16)).astype(
+            np.float64)
+        finite = np.isfinite(v)
+        byte, _ = _e4m3_encode(np.where(finite, np.abs(v), 0.0) / float(g))
+    lut = np.where(v < 0, byte | np.uint8(0x80), byte).astype(np.uint8)
+    lut[~finite] = 0x7F
+    return lut[wbits], float(g)
 
 
 # ---------------------------------------------------------------------------

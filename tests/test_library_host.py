@@ -194,3 +194,20 @@ def test_learn_checks_reject_before_any_launch(dvl):
     assert L.dvl_learn_rows(ctypes.byref(sliced), ok, 2, 0, 0x1000, None, 0x2000, None) == 1
     nv = _head(dtype=1, scales=None)  # NVFP4 without scales
     assert L.dvl_learn_rows(ctypes.byref(nv), ok, 2, 0, 0x1000, None, 0x2000, None) == 1
+
+
+def test_fp8_head_checks(dvl):
+    # FP8 heads take no per-block scales; a valid FP8 head passes the head
+    # checks (the out-of-range id is what a trim then refuses)
+    from draft_vocab_lm_gb300._native import lib, DVL_FP8
+    L = lib()
+    ids = (ctypes.c_int32 * 2)(4, 100)
+    fp8 = _head(dtype=DVL_FP8)
+    assert L.dvl_learn_rows(ctypes.byref(fp8), ids, 2, 0, 0x1000, None, 0x2000, None) == 2
+    with_scales = _head(dtype=DVL_FP8, scales=0x7000)
+    assert L.dvl_learn_rows(ctypes.byref(with_scales), ids, 2, 0, 0x1000, None, 0x2000, None) == 1
+    assert L.dvl_score_ids(ctypes.byref(with_scales), 0x3000, 1, 0x2000, 4, 0x4000, None) == 1
+    bf16_scales = _head(scales=0x7000)
+    assert L.dvl_score_ids(ctypes.byref(bf16_scales), 0x3000, 1, 0x2000, 4, 0x4000, None) == 1
+    unknown = _head(dtype=3)
+    assert L.dvl_score_ids(ctypes.byref(unknown), 0x3000, 1, 0x2000, 4, 0x4000, None) == 1
