@@ -55,11 +55,13 @@ constexpr int kRows = 16;      // head rows per warp group (MMA M)
 constexpr int kChunk = 128;    // weights per row per k chunk
 constexpr int kFmtNvfp4 = 0, kFmtFp8 = 1;
 // 16-byte code loads per row per chunk per lane, code bytes per row per
-// k chunk, and k chunks of loads in flight per lane (the same ~4.5 KB per
-// warp for both formats)
+// k chunk, and k chunks of loads in flight per lane: 4 (measured against 2
+// and 5; ~4.5 KB per warp for NVFP4, ~8 KB for FP8), except 2 for FP8
+// top-k at run-time widths, whose lists leave no room for a deeper ring
 template <int FMT> __host__ __device__ constexpr int q_words() { return FMT == kFmtFp8 ? 2 : 1; }
 template <int FMT> __host__ __device__ constexpr int chunk_bytes() { return FMT == kFmtFp8 ? 128 : 64; }
-template <int FMT> __host__ __device__ constexpr int ring_depth() { return FMT == kFmtFp8 ? 2 : 4; }
+template <int FMT, int KC, int KM>
+__host__ __device__ constexpr int ring_depth() { return FMT == kFmtFp8 && KC == 0 && KM > 1 ? 2 : 4; }
 constexpr int kLists = kWarps * 8;  // candidate lists per hidden row (8 row pairs per warp)
 
 // Four bytes of codes -> four f16x2 (byte t: low nibble in the low half).
@@ -128,7 +130,7 @@ __host__ __device__ inline size_t lowbit_h_bytes(int Kpad, int M) { return (size
 template <int FMT, int M, int KM, int KC>
 __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const ArgmaxArgs a)
 {
-    constexpr int kNB = ring_depth<FMT>(), kQW = q_words<FMT>();
+    constexpr int kNB = ring_depth<FMT, KC, KM>(), kQW = q_words<FMT>();
     constexpr bool kNv = FMT == kFmtNvfp4;
     extern __shared__ __align__(16) unsigned char smem[];
     const int K = KC > 0 ? KC : a.K;
