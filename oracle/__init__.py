@@ -90,6 +90,10 @@ def _load():
     lib.oracle_score_ids_nvfp4.argtypes = [p, p, ctypes.c_float, i64, i64, i64, p, i64, p,
                                            i64, p]
     lib.oracle_score_ids_nvfp4.restype = None
+    lib.oracle_quantize_nvfp4.argtypes = [p, i64, i64, p, p]
+    lib.oracle_quantize_nvfp4.restype = ctypes.c_float
+    lib.oracle_quantize_fp8.argtypes = [p, i64, i64, p]
+    lib.oracle_quantize_fp8.restype = ctypes.c_float
     lib.oracle_topk.argtypes = [p, i64, i64, p, ctypes.c_int, p, p, p]
     lib.oracle_topk.restype = None
     lib.oracle_check_trim.argtypes = [p, i64, i64, p, i64, p, p]
@@ -222,6 +226,27 @@ def score_ids_fp8(q: np.ndarray, g: float, h: np.ndarray, ids: np.ndarray, id_ba
     _load().oracle_score_ids_fp8(_ptr(q), float(g), N, K, int(id_base), _ptr(h), M, _ptr(ids),
                                  c, _ptr(out))
     return out
+
+
+def quantize_nvfp4(w: np.ndarray):
+    """Requantize a bf16 head [N][K] (bits) to NVFP4 by the plain recipe:
+    returns (codes uint8[N][K/2], scales uint8[N][K/16], g)."""
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    N, K = w.shape
+    q = np.empty((N, K // 2), dtype=np.uint8)
+    sc = np.empty((N, K // 16), dtype=np.uint8)
+    g = _load().oracle_quantize_nvfp4(_ptr(w), N, K, _ptr(q), _ptr(sc))
+    return q, sc, float(g)
+
+
+def quantize_fp8(w: np.ndarray):
+    """Requantize a bf16 head [N][K] (bits) to FP8 E4M3 with one tensor
+    scale: returns (codes uint8[N][K], g)."""
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    N, K = w.shape
+    q = np.empty((N, K), dtype=np.uint8)
+    g = _load().oracle_quantize_fp8(_ptr(w), N, K, _ptr(q))
+    return q, float(g)
 
 
 def nvfp4_weight(q, scales, g, n, k) -> float:

@@ -39,6 +39,16 @@
  *       MTP drafts": a drafter shipping an FP8 head).  The layout (row-major
  *       codes, one byte per weight, one fp32 tensor scale) is the reading
  *       this project adopts.
+ *   requantization of a bf16 head ("Masked MTP drafts": the trimmed head
+ *       requantized to NVFP4 at load, at no measured acceptance cost; the
+ *       pages give no recipe, so the one below is the plainest reading, in
+ *       fp32 with each operation rounded once, in the order written):
+ *       NVFP4: g = amax / (6 * 448); per 16-weight block s = RNE_e4m3(
+ *       amax_b / (6 g)); code = RNE_e2m1(w / (s g)), all codes 0 when s is 0.
+ *       FP8: g = amax / 448; code = RNE_e4m3(w / g).  RNE: the nearest value
+ *       of the format, ties to the code with an even last mantissa bit,
+ *       magnitudes above the largest value saturating to it; the sign bit
+ *       is the sign of the quotient (so -0 keeps its sign).
  *   trim check: W_trim[i] == W_full[ranks[i]] byte for byte, d2t[i] ==
  *       ranks[i] ("Masked MTP drafts": a ranks list next to the model, the
  *       head weight trimmed at load).
@@ -262,6 +272,85 @@ int oracle_logits_fp8(const uint8_t *q, float g, int64_t N, int64_t K, const uin
     j.h = h;
     j.logits = logits;
     return run_logits(j, nthreads);
+}
+
+/* ------------------------------------------------------------------ */
+/* Requantization: the nearest code by search over the format's values. */
+/* ------------------------------------------------------------------ */
+
+/* Non-negative x -> the code among 0 .. ncodes - 1 (values increasing with
+ * the code) whose value is nearest, ties to the even code; above the
+ * largest value that value is the nearest, which is the saturation. */
+static uint8_t nearest_code(float x, float (*decode)(uint8_t), int ncodes)
+{
+    uint8_t best = 0;
+    double bd = fabs((double)x - (double)decode(0));
+    for (int c = 1; c < ncodes; ++c) {
+        double d = fabs((double)x - (double)decode((uint8_t)c));
+        if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) != 0)) {
+            best = (uint8_t)c;
+            bd = d;
+        }
+    }
+    return best;
+}
+
+static uint8_t rne_e2m1(float x) /* 4-bit code, sign in bit 3 */
+{
+    uint8_t c = nearest_code(fabsf(x), oracle_e2m1, 8);
+    return signbit(x) ? (uint8_t)(c | 8) : c;
+}
+
+static uint8_t rne_e4m3(float x) /* sign in bit 7; 0x7E = 448 is the largest */
+{
+    uint8_t c = nearest_code(fabsf(x), oracle_e4m3, 127);
+    return signbit(x) ? (uint8_t)(c | 0x80) : c;
+}
+
+static float abs_max_bf16(const uint16_t *w, int64_t n)
+{
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(oracle_bf16_to_f32(w[i]));
+        if (a > m)
+            m = a;
+    }
+    return m;
+}
+
+float oracle_quantize_nvfp4(const uint16_t *w, int64_t N, int64_t K, uint8_t *q,
+                            uint8_t *scales)
+{
+    float amax = abs_max_bf16(w, N * K);
+    float g = amax > 0.0f ? amax / 2688.0f : 1.0f; /* 2688 = 6 * 448 */
+    float six_g = 6.0f * g;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t b = 0; b < K / 16; ++b) {
+            const uint16_t *wb = w + n * K + b * 16;
+            float amax_b = abs_max_bf16(wb, 16);
+            uint8_t sb = rne_e4m3(amax_b / six_g);
+            scales[n * (K / 16) + b] = sb;
+            float sg = oracle_e4m3(sb) * g;
+            for (int j = 0; j < 16; j += 2) {
+                uint8_t lo = 0, hi = 0;
+                if (oracle_e4m3(sb) != 0.0f) {
+                    lo = rne_e2m1(oracle_bf16_to_f32(wb[j]) / sg);
+                    hi = rne_e2m1(oracle_bf16_to_f32(wb[j + 1]) / sg);
+                }
+                q[n * (K / 2) + (b * 16 + j) / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+    return g;
+}
+
+float oracle_quantize_fp8(const uint16_t *w, int64_t N, int64_t K, uint8_t *q)
+{
+    float amax = abs_max_bf16(w, N * K);
+    float g = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int64_t i = 0; i < N * K; ++i)
+        q[i] = rne_e4m3(oracle_bf16_to_f32(w[i]) / g);
+    return g;
 }
 
 /* ------------------------------------------------------------------ */

@@ -35,6 +35,9 @@ void oracle_score_ids_bf16(const uint16_t *w, int64_t N, int64_t K, int64_t id_b
 void oracle_score_ids_nvfp4(const uint8_t *q, const uint8_t *scales, float g, int64_t N,
                             int64_t K, int64_t id_base, const uint16_t *h, int64_t M,
                             const int32_t *ids, int64_t c, float *out);
+float oracle_quantize_nvfp4(const uint16_t *w, int64_t N, int64_t K, uint8_t *q,
+                            uint8_t *scales);
+float oracle_quantize_fp8(const uint16_t *w, int64_t N, int64_t K, uint8_t *q);
 void oracle_topk(const float *logits, int64_t N, int64_t M, const int32_t *d2t, int k,
                  int32_t *ids, float *vals, int64_t *rows);
 
