@@ -279,31 +279,51 @@ int oracle_logits_fp8(const uint8_t *q, float g, int64_t N, int64_t K, const uin
 /* ------------------------------------------------------------------ */
 
 /* Non-negative x -> the code among 0 .. ncodes - 1 (values increasing with
- * the code) whose value is nearest, ties to the even code; above the
- * largest value that value is the nearest, which is the saturation. */
-static uint8_t nearest_code(float x, float (*decode)(uint8_t), int ncodes)
+ * the code; vals[c] its value) whose value is nearest, ties to the even
+ * code; above the largest value that value is the nearest, which is the
+ * saturation.  Bisection finds the neighbours lo <= x < lo + 1. */
+static uint8_t nearest_code(float x, const float *vals, int ncodes)
 {
-    uint8_t best = 0;
-    double bd = fabs((double)x - (double)decode(0));
-    for (int c = 1; c < ncodes; ++c) {
-        double d = fabs((double)x - (double)decode((uint8_t)c));
-        if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) != 0)) {
-            best = (uint8_t)c;
-            bd = d;
-        }
+    if (x >= vals[ncodes - 1])
+        return (uint8_t)(ncodes - 1);
+    int lo = 0, hi = ncodes - 1; /* vals[lo] <= x < vals[hi] */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (vals[mid] <= x)
+            lo = mid;
+        else
+            hi = mid;
     }
-    return best;
+    double dlo = (double)x - (double)vals[lo], dhi = (double)vals[hi] - (double)x;
+    if (dlo < dhi)
+        return (uint8_t)lo;
+    if (dhi < dlo)
+        return (uint8_t)hi;
+    return (uint8_t)((lo & 1) == 0 ? lo : hi); /* tie: the even code */
+}
+
+/* The non-negative values of each format, by code, from the decoders above. */
+static float g_e2m1_vals[8], g_e4m3_vals[127];
+static pthread_once_t g_vals_once = PTHREAD_ONCE_INIT;
+static void fill_vals(void)
+{
+    for (int c = 0; c < 8; ++c)
+        g_e2m1_vals[c] = oracle_e2m1((uint8_t)c);
+    for (int c = 0; c < 127; ++c)
+        g_e4m3_vals[c] = oracle_e4m3((uint8_t)c);
 }
 
 static uint8_t rne_e2m1(float x) /* 4-bit code, sign in bit 3 */
 {
-    uint8_t c = nearest_code(fabsf(x), oracle_e2m1, 8);
+    pthread_once(&g_vals_once, fill_vals);
+    uint8_t c = nearest_code(fabsf(x), g_e2m1_vals, 8);
     return signbit(x) ? (uint8_t)(c | 8) : c;
 }
 
 static uint8_t rne_e4m3(float x) /* sign in bit 7; 0x7E = 448 is the largest */
 {
-    uint8_t c = nearest_code(fabsf(x), oracle_e4m3, 127);
+    pthread_once(&g_vals_once, fill_vals);
+    uint8_t c = nearest_code(fabsf(x), g_e4m3_vals, 127);
     return signbit(x) ? (uint8_t)(c | 0x80) : c;
 }
 
