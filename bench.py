@@ -551,6 +551,15 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
                                     {"note": "load-time gather incl. host rank check + H2D of d2t"})
     w_trim3, _, d2t3, _ = dvl.trim_head(wf, ranks)
     del wf
+    # requantizing the trimmed head at load (two kernels and one host read
+    # of the head's maximum; wall time around the call, synchronized)
+    for fmt in ("nvfp4", "fp8"):
+        def quant(i, fmt=fmt):
+            dvl.quantize_head(w_trim3, fmt, ws=ws)
+        tq = repeat_stats(torch, quant, 3, R)
+        out[f"c3_quantize_{fmt}_32k"] = entry(RL.quantize_bytes(len(ranks), wl3.K, fmt), *tq, peak,
+                                              {"note": "load time; includes the host read of "
+                                                       "the maximum (one stream sync)"})
     b3 = RL.call_bytes(len(ranks), wl3.K, 1)
     R3 = rotation_copies(b3, l2)
     torch.cuda.synchronize()

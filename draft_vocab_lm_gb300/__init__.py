@@ -28,6 +28,7 @@ from ._native import (DVL_BF16, DVL_FP8, DVL_HEAD_STATIC, DVL_K_MULTIPLE, DVL_MA
 
 __all__ = [
     "Head", "DvlError", "draft_argmax", "draft_topk", "score_ids", "trim_head", "learn_rows",
+    "quantize_head",
     "Shortlist", "workspace_bytes",
     "make_workspace", "workspace_init", "histogram", "build_ranks", "union_sorted",
     "read_ranks_txt", "write_ranks_txt", "roofline", "version",
@@ -255,6 +256,32 @@ def trim_head(w_full, ranks, *, scales=None, fmt=None, stream=None):
                               d2t.data_ptr(), ctypes.byref(dup),
                               _stream_handle(stream, w_full.device)))
     return w_trim, s_trim, d2t, int(dup.value)
+
+
+def quantize_head(w, fmt: str = "nvfp4", *, ws=None, stream=None):
+    """Requantize a bf16 head [N][K] (CUDA) to NVFP4 or FP8 on the device
+    (dvl_quantize_head; synchronizes the stream once, to read the head's
+    maximum back).  Returns (codes, scales or None, global_scale); pass them
+    to Head(codes, scales=..., global_scale=..., fmt=fmt)."""
+    torch = _torch()
+    src = Head(w)
+    N, K = src.N, src.K
+    if fmt == "nvfp4":
+        dtype, codes = DVL_NVFP4, torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+        scales = torch.empty((N, K // 16), dtype=torch.uint8, device=w.device)
+    elif fmt == "fp8":
+        dtype, codes, scales = DVL_FP8, torch.empty((N, K), dtype=torch.uint8, device=w.device), None
+    else:
+        raise ValueError("fmt must be nvfp4 or fp8")
+    if ws is None:
+        ws = make_workspace(1, 1, device=w.device, stream=stream)
+    g = ctypes.c_float(0.0)
+    check("dvl_quantize_head",
+          lib().dvl_quantize_head(ctypes.byref(src.struct()), dtype, codes.data_ptr(),
+                                  scales.data_ptr() if scales is not None else None,
+                                  ctypes.byref(g), ws.data_ptr(), ws.numel(),
+                                  _stream_handle(stream, w.device)))
+    return codes, scales, float(g.value)
 
 
 def learn_rows(w_full, ids, w_trim, d2t, row0: int, *, scales=None, scales_trim=None,

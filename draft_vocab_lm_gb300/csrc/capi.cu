@@ -332,6 +332,32 @@ dvl_status dvl_trim_head(const dvl_head *full, const int32_t *ranks, int32_t n_r
     return gather_rows(full, ranks, n_ranks, 0, w_trim, scales_trim, d2t, n_duplicates, stream);
 }
 
+dvl_status dvl_quantize_head(const dvl_head *src, int32_t dtype, void *codes, uint8_t *scales,
+                             float *global_scale, void *ws, size_t ws_bytes, void *stream)
+{
+    dvl_status st = check_head(src);
+    if (st != DVL_OK)
+        return st;
+    if (src->dtype != DVL_BF16 || (dtype != DVL_NVFP4 && dtype != DVL_FP8))
+        return DVL_ERR_INVALID_ARG;
+    if (!codes || !aligned(codes, 16) || !global_scale)
+        return DVL_ERR_INVALID_ARG;
+    if ((dtype == DVL_NVFP4) != (scales != nullptr) || (scales && !aligned(scales, 16)))
+        return DVL_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, 16) || ws_bytes < dvl_workspace_bytes(1, 1))
+        return DVL_ERR_WORKSPACE;
+    float g = 1.0f;
+    cudaError_t e = launch_quantize(static_cast<const uint16_t *>(src->w),
+                                    (long long)src->N * src->K, dtype,
+                                    static_cast<uint8_t *>(codes), scales,
+                                    static_cast<unsigned char *>(ws),
+                                    static_cast<cudaStream_t>(stream), &g);
+    if (e != cudaSuccess)
+        return cuda_failed(e);
+    *global_scale = g;
+    return DVL_OK;
+}
+
 dvl_status dvl_learn_rows(const dvl_head *full, const int32_t *ids, int32_t n, int32_t row0,
                           void *w_trim, uint8_t *scales_trim, int32_t *d2t, void *stream)
 {

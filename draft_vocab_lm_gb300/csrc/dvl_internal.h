@@ -15,6 +15,7 @@ namespace dvl {
 constexpr int kMaxCtas = 1024;            // grid cap of every reducing kernel
 constexpr size_t kWsTicket = 0;           // uint32: blocks finished so far
 constexpr size_t kWsStatus = 4;           // uint32: reserved for device checks
+constexpr size_t kWsAmax = 8;             // uint32: a head's max |w| while it is requantized
 constexpr size_t kWsBest = 256;           // uint64[DVL_MAX_M]: best key per row (k = 1)
 constexpr size_t kWsSlots = 512;          // uint64[kMaxCtas][M][kmax] (k > 1)
 
@@ -78,6 +79,11 @@ struct ScoreArgs {
     float *out;               // [M][c]
 };
 cudaError_t launch_score(const ScoreArgs &a, cudaStream_t s);
+
+// Requantize a bf16 head of n weights to NVFP4 or FP8 (dtype); reads the
+// head's maximum back (synchronizing s) and returns the tensor scale in g_out.
+cudaError_t launch_quantize(const uint16_t *w, long long n, int dtype, uint8_t *codes,
+                            uint8_t *scales, unsigned char *ws, cudaStream_t s, float *g_out);
 
 cudaError_t launch_trim_rows(const unsigned char *src, int64_t src_row_bytes,
                              unsigned char *dst, const int32_t *ranks, int n,

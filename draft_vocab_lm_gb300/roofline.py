@@ -43,6 +43,12 @@ def score_bytes(M: int, c: int, K: int, dtype: str = "bf16") -> int:
     return M * c * row + M * K * 2 + M * c * 8
 
 
+def quantize_bytes(N: int, K: int, dtype: str) -> int:
+    """Algorithmic bytes of requantizing a bf16 N x K head: the head read
+    twice (its maximum, then the codes) and the NVFP4 or FP8 head written."""
+    return 2 * N * K * 2 + head_bytes(N, K, dtype) - 4
+
+
 def call_flops(N: int, K: int, M: int) -> int:
     """Multiply-adds of the projection, counted as 2 flops each."""
     return 2 * M * N * K

@@ -244,6 +244,30 @@ dvl_status dvl_trim_head(const dvl_head *full, const int32_t *ranks, int32_t n_r
                          void *w_trim, uint8_t *scales_trim, int32_t *d2t,
                          int32_t *n_duplicates, void *stream);
 
+/* Requantize a bf16 head to NVFP4 or FP8 at load ("Masked MTP drafts": the
+ * trimmed head requantized to NVFP4 at no measured acceptance cost; the
+ * pages give no recipe).  In fp32, each operation rounded once, in order:
+ *   NVFP4: g = amax / (6 * 448); per 16 consecutive weights of a row
+ *          s = RNE_e4m3(amax_b / (6 g)), code = RNE_e2m1(w / (s g)), all
+ *          codes 0 when s is 0;
+ *   FP8:   g = amax / 448; code = RNE_e4m3(w / g);
+ * amax is the head's largest |w| (g = 1 for an all-zero head); RNE rounds
+ * to the nearest value of the format, ties to even, saturating at its
+ * largest finite value; a code's sign is its quotient's.  The weights must
+ * be finite.
+ *   src:    a bf16 head (only dtype, N, K and w are read).
+ *   dtype:  DVL_NVFP4 or DVL_FP8.
+ *   codes:  device, 16-byte aligned: NVFP4 [N][K/2] (low nibble = even k) or
+ *           FP8 [N][K].
+ *   scales: device, 16-byte aligned NVFP4 E4M3 [N][K/16]; NULL for FP8.
+ *   global_scale: HOST float (out): g.
+ *   ws:     a workspace from dvl_workspace_init (at least
+ *           dvl_workspace_bytes(1, 1) bytes); left as it was found.
+ * This load-time call synchronizes `stream` once, to read amax back.
+ * Errors: DVL_ERR_INVALID_ARG, DVL_ERR_WORKSPACE, DVL_ERR_CUDA. */
+dvl_status dvl_quantize_head(const dvl_head *src, int32_t dtype, void *codes, uint8_t *scales,
+                             float *global_scale, void *ws, size_t ws_bytes, void *stream);
+
 /* Learn escaped ids into spare rows of a trimmed head while serving ("Masked
  * MTP drafts", section "Update (November 2026)": a static trim can miss;
  * the server learns the escaped ids into spare head rows).  For i < n:

@@ -211,3 +211,21 @@ def test_fp8_head_checks(dvl):
     assert L.dvl_score_ids(ctypes.byref(bf16_scales), 0x3000, 1, 0x2000, 4, 0x4000, None) == 1
     unknown = _head(dtype=3)
     assert L.dvl_score_ids(ctypes.byref(unknown), 0x3000, 1, 0x2000, 4, 0x4000, None) == 1
+
+
+def test_quantize_checks_reject_before_any_launch(dvl):
+    from draft_vocab_lm_gb300._native import lib, DVL_NVFP4, DVL_FP8
+    L = lib()
+    g = ctypes.c_float(0.0)
+    h = _head()
+    ok_ws = 0x5000
+    # target format, source format, pointers, scales presence, workspace
+    assert L.dvl_quantize_head(ctypes.byref(h), 0, 0x1000, None, ctypes.byref(g), ok_ws, 512, None) == 1
+    assert L.dvl_quantize_head(ctypes.byref(_head(dtype=DVL_FP8)), DVL_FP8, 0x1000, None,
+                               ctypes.byref(g), ok_ws, 512, None) == 1
+    assert L.dvl_quantize_head(ctypes.byref(h), DVL_FP8, 0x1008, None, ctypes.byref(g), ok_ws, 512, None) == 1
+    assert L.dvl_quantize_head(ctypes.byref(h), DVL_FP8, 0x1000, 0x2000, ctypes.byref(g), ok_ws, 512, None) == 1
+    assert L.dvl_quantize_head(ctypes.byref(h), DVL_NVFP4, 0x1000, None, ctypes.byref(g), ok_ws, 512, None) == 1
+    assert L.dvl_quantize_head(ctypes.byref(h), DVL_NVFP4, 0x1000, 0x2000, None, ok_ws, 512, None) == 1
+    assert L.dvl_quantize_head(ctypes.byref(h), DVL_FP8, 0x1000, None, ctypes.byref(g), None, 512, None) == 4
+    assert L.dvl_quantize_head(ctypes.byref(h), DVL_FP8, 0x1000, None, ctypes.byref(g), ok_ws, 100, None) == 4
