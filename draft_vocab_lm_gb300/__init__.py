@@ -27,7 +27,7 @@ from ._native import (DVL_BF16, DVL_FP8, DVL_HEAD_STATIC, DVL_K_MULTIPLE, DVL_MA
                       DVL_MAX_TOPK, DVL_NVFP4, DvlError, DvlHead, check, lib)
 
 __all__ = [
-    "Head", "DvlError", "draft_argmax", "draft_topk", "score_ids", "trim_head", "learn_rows",
+    "Head", "DvlError", "workspace_status", "draft_argmax", "draft_topk", "score_ids", "trim_head", "learn_rows",
     "quantize_head",
     "Shortlist", "workspace_bytes",
     "make_workspace", "workspace_init", "histogram", "build_ranks", "union_sorted",
@@ -157,6 +157,18 @@ def workspace_init(ws, stream=None) -> None:
     check("dvl_workspace_init",
           lib().dvl_workspace_init(ws.data_ptr(), ws.numel() * ws.element_size(),
                                    _stream_handle(stream, ws.device)))
+
+
+def workspace_status(ws, stream=None) -> int:
+    """Device-side failures recorded in `ws` since the last read, as a bitmask
+    of 1 << status (DVL_ERR_TIMEOUT: a bounded device wait gave up and that
+    call's results are not valid); reading synchronizes the stream and
+    clears the word."""
+    bits = ctypes.c_uint32(0)
+    check("dvl_workspace_status",
+          lib().dvl_workspace_status(ws.data_ptr(), ctypes.byref(bits),
+                                     _stream_handle(stream, ws.device)))
+    return int(bits.value)
 
 
 def make_workspace(M: int = DVL_MAX_M, k: int = DVL_MAX_TOPK, device=None, stream=None):

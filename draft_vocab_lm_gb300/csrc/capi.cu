@@ -285,6 +285,24 @@ dvl_status dvl_workspace_init(void *ws, size_t bytes, void *stream)
     return DVL_OK;
 }
 
+dvl_status dvl_workspace_status(void *ws, uint32_t *status_bits, void *stream)
+{
+    if (!ws || !aligned(ws, 16) || !status_bits)
+        return DVL_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char *word = static_cast<unsigned char *>(ws) + kWsStatus;
+    uint32_t bits = 0u;
+    cudaError_t e = cudaMemcpyAsync(&bits, word, sizeof bits, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(word, 0, sizeof bits, s);
+    if (e != cudaSuccess)
+        return cuda_failed(e);
+    *status_bits = bits;
+    return DVL_OK;
+}
+
 dvl_status dvl_draft_argmax(const dvl_head *head, const void *h, int32_t M, int32_t *ids,
                             float *max_logit, void *ws, size_t ws_bytes, void *stream)
 {

@@ -130,6 +130,17 @@ size_t dvl_workspace_bytes(int32_t M, int32_t k);
  * call that will use it. */
 dvl_status dvl_workspace_init(void *ws, size_t bytes, void *stream);
 
+/* Device-side failures recorded in a workspace since it was last read: a
+ * bitmask with bit (1 << s) set for each dvl_status s a kernel reported.
+ * Today the only one is DVL_ERR_TIMEOUT: a bounded wait of the tensor-core
+ * argmax gave up, and that call's results are not valid.  The status word
+ * is read after the work already enqueued on `stream` (this synchronizes
+ * `stream`), then cleared on `stream`.
+ *   ws:          a workspace from dvl_workspace_init.
+ *   status_bits: HOST (out).
+ * Errors: DVL_ERR_INVALID_ARG, DVL_ERR_CUDA. */
+dvl_status dvl_workspace_status(void *ws, uint32_t *status_bits, void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* The hot path                                                           */
 /* ---------------------------------------------------------------------- */

@@ -258,3 +258,23 @@ def test_trim_then_argmax_without_synchronizing(dvl, oracle_mod):
         o_ids, o_vals = oracle_mod.argmax(L, ranks)
         assert np.array_equal(ids.cpu().numpy(), o_ids), it
         assert np.array_equal(vals.cpu().numpy(), o_vals), it
+
+
+def test_workspace_status_reads_and_clears(dvl, oracle_mod):
+    # a fresh workspace reports nothing; a status bit written from the host
+    # (standing in for a kernel's record) is reported once, then cleared;
+    # ordinary calls, the tensor-core one included, record nothing
+    ws = dvl.make_workspace(8, 4)
+    assert dvl.workspace_status(ws) == 0
+    ws[4:8].view(torch.int32)[0] = 1 << 6  # DVL_ERR_TIMEOUT
+    assert dvl.workspace_status(ws) == 1 << 6
+    assert dvl.workspace_status(ws) == 0
+    rng = np.random.default_rng(12)
+    w = int_bf16(rng, (3000, 256))
+    head = dvl.Head(dev(w))
+    for M in (1, 8):
+        h = int_bf16(rng, (M, 256))
+        L, _ = oracle_mod.logits_bf16(w, h)
+        ids, _ = dvl.draft_argmax(head, dev(h), ws=ws)
+        assert np.array_equal(ids.cpu().numpy(), oracle_mod.argmax(L)[0])
+    assert dvl.workspace_status(ws) == 0
