@@ -21,13 +21,20 @@ cudaError_t launch_argmax_lowbit(const ArgmaxArgs &a_in, int dtype, int M, int k
     using namespace lowbit;
     ArgmaxArgs a = a_in;
     a.Kpad = kpad_of(a.K);
-    // argmax at the unrolled widths: one base pointer per group with
-    // immediate offsets (measured 29.0 -> 20.4 us on a 32k x 5,120 NVFP4 head)
-    const bool kc = kmax == 1 && M <= 4 && (a.K == 5120 || a.K == 2560);
-    if (dtype == DVL_NVFP4)
-        return kc ? launch_kc<kFmtNvfp4>(a, M, s) : launch_rt<kFmtNvfp4>(a, M, kmax, s);
-    if (dtype == DVL_FP8)
-        return kc ? launch_kc<kFmtFp8>(a, M, s) : launch_rt<kFmtFp8>(a, M, kmax, s);
+    // argmax and top-k at the unrolled widths: one base pointer per group
+    // with immediate offsets (measured 29.0 -> 20.4 us on a 32k x 5,120 NVFP4
+    // head)
+    const bool kc = M <= 4 && (a.K == 5120 || a.K == 2560);
+    if (dtype == DVL_NVFP4) {
+        if (kc)
+            return kmax == 1 ? launch_kc<kFmtNvfp4, 1>(a, M, s) : launch_kc<kFmtNvfp4, 4>(a, M, s);
+        return launch_rt<kFmtNvfp4>(a, M, kmax, s);
+    }
+    if (dtype == DVL_FP8) {
+        if (kc)
+            return kmax == 1 ? launch_kc<kFmtFp8, 1>(a, M, s) : launch_kc<kFmtFp8, 4>(a, M, s);
+        return launch_rt<kFmtFp8>(a, M, kmax, s);
+    }
     return cudaErrorInvalidValue;
 }
 

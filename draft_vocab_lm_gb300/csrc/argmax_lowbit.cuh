@@ -57,11 +57,11 @@ constexpr int kFmtNvfp4 = 0, kFmtFp8 = 1;
 // 16-byte code loads per row per chunk per lane, code bytes per row per
 // k chunk, and k chunks of loads in flight per lane: 4 (measured against 2
 // and 5; ~4.5 KB per warp for NVFP4, ~8 KB for FP8), except 2 for FP8
-// top-k at run-time widths, whose lists leave no room for a deeper ring
+// top-k, whose lists leave no room for a deeper ring
 template <int FMT> __host__ __device__ constexpr int q_words() { return FMT == kFmtFp8 ? 2 : 1; }
 template <int FMT> __host__ __device__ constexpr int chunk_bytes() { return FMT == kFmtFp8 ? 128 : 64; }
 template <int FMT, int KC, int KM>
-__host__ __device__ constexpr int ring_depth() { return FMT == kFmtFp8 && KC == 0 && KM > 1 ? 2 : 4; }
+__host__ __device__ constexpr int ring_depth() { return FMT == kFmtFp8 && KM > 1 ? 2 : 4; }
 constexpr int kLists = kWarps * 8;  // candidate lists per hidden row (8 row pairs per warp)
 
 // Four bytes of codes -> four f16x2 (byte t: low nibble in the low half).
@@ -536,9 +536,6 @@ cudaError_t launch_one(const ArgmaxArgs &a, cudaStream_t s)
     return launch_pdl(kern, (unsigned)grid, kThreads, smem, s, a);
 }
 
-// The unrolled widths are instantiated for argmax only; top-k takes the
-// run-time-K loop (keeps the build small).
-
 inline int kpad_of(int K) { return (K + kChunk - 1) / kChunk * kChunk; }
 
 template <int FMT, int KM, int KC>
@@ -557,24 +554,24 @@ cudaError_t dispatch_m(const ArgmaxArgs &a, int M, cudaStream_t s)
     }
 }
 
-// argmax at the unrolled widths (K = 2,560 or 5,120, M <= 4): one base
-// pointer per group with immediate offsets.
-template <int FMT>
+// argmax (KM = 1) or top-k (KM = 4) at the unrolled widths (K = 2,560 or
+// 5,120, M <= 4): one base pointer per group with immediate offsets.
+template <int FMT, int KM>
 cudaError_t launch_kc(const ArgmaxArgs &a, int M, cudaStream_t s)
 {
     if (a.K == 5120) {
         switch (M) {
-        case 1: return launch_one<FMT, 1, 1, 5120>(a, s);
-        case 2: return launch_one<FMT, 2, 1, 5120>(a, s);
-        case 3: return launch_one<FMT, 3, 1, 5120>(a, s);
-        case 4: return launch_one<FMT, 4, 1, 5120>(a, s);
+        case 1: return launch_one<FMT, 1, KM, 5120>(a, s);
+        case 2: return launch_one<FMT, 2, KM, 5120>(a, s);
+        case 3: return launch_one<FMT, 3, KM, 5120>(a, s);
+        case 4: return launch_one<FMT, 4, KM, 5120>(a, s);
         }
     } else if (a.K == 2560) {
         switch (M) {
-        case 1: return launch_one<FMT, 1, 1, 2560>(a, s);
-        case 2: return launch_one<FMT, 2, 1, 2560>(a, s);
-        case 3: return launch_one<FMT, 3, 1, 2560>(a, s);
-        case 4: return launch_one<FMT, 4, 1, 2560>(a, s);
+        case 1: return launch_one<FMT, 1, KM, 2560>(a, s);
+        case 2: return launch_one<FMT, 2, KM, 2560>(a, s);
+        case 3: return launch_one<FMT, 3, KM, 2560>(a, s);
+        case 4: return launch_one<FMT, 4, KM, 2560>(a, s);
         }
     }
     return cudaErrorInvalidValue;
@@ -589,8 +586,10 @@ cudaError_t launch_rt(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s)
 
 // Each format's instantiations live in a translation unit of their own
 // (compiled in parallel).
-extern template cudaError_t launch_kc<kFmtNvfp4>(const ArgmaxArgs &, int, cudaStream_t);
-extern template cudaError_t launch_kc<kFmtFp8>(const ArgmaxArgs &, int, cudaStream_t);
+extern template cudaError_t launch_kc<kFmtNvfp4, 1>(const ArgmaxArgs &, int, cudaStream_t);
+extern template cudaError_t launch_kc<kFmtFp8, 1>(const ArgmaxArgs &, int, cudaStream_t);
+extern template cudaError_t launch_kc<kFmtNvfp4, 4>(const ArgmaxArgs &, int, cudaStream_t);
+extern template cudaError_t launch_kc<kFmtFp8, 4>(const ArgmaxArgs &, int, cudaStream_t);
 extern template cudaError_t launch_rt<kFmtNvfp4>(const ArgmaxArgs &, int, int, cudaStream_t);
 extern template cudaError_t launch_rt<kFmtFp8>(const ArgmaxArgs &, int, int, cudaStream_t);
 

@@ -5,7 +5,7 @@
 namespace dvl {
 namespace lowbit {
 
-template cudaError_t launch_kc<kFmtNvfp4>(const ArgmaxArgs &, int, cudaStream_t);
+template cudaError_t launch_kc<kFmtNvfp4, 1>(const ArgmaxArgs &, int, cudaStream_t);
 
 }  // namespace lowbit
 }  // namespace dvl

@@ -5,7 +5,7 @@
 namespace dvl {
 namespace lowbit {
 
-template cudaError_t launch_kc<kFmtFp8>(const ArgmaxArgs &, int, cudaStream_t);
+template cudaError_t launch_kc<kFmtFp8, 1>(const ArgmaxArgs &, int, cudaStream_t);
 
 }  // namespace lowbit
 }  // namespace dvl
