@@ -228,10 +228,10 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
         // Every warp takes part: warp w merges row w % M over a share of the
         // blocks, its lanes loading kBatch blocks' slots before inserting any
         // (one L2 round trip per batch rather than per block); then one warp
-        // per row merges the warps' lists.  The reducing kernels have
-        // M <= nwarps <= kFinWarps whenever k > 1.
+        // per row merges the warps' lists (at most 32 of them, one per lane).
+        // The reducing kernels have M <= nwarps whenever k > 1.
         constexpr int kBatch = 4;
-        constexpr int kFinWarps = 8;
+        constexpr int kFinWarps = 32;  // the most warps a block can have
         __shared__ uint64_t s_fin[kFinWarps][KM];
         const int wpm = nwarps / M;  // warps per hidden row
         const int m = warp % M, q = warp / M;
