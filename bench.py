@@ -609,6 +609,11 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
         out[f"c4_union53k_M{M}_argmax"] = entry(
             b4, *t, peak, {"l2_rotation_copies": R4,
                            "TFLOPs": round(RL.call_flops(wl4.N, wl4.K, M) / t[0] / 1e12, 2)})
+        if M in (8, 32):
+            t = repeat_stats(torch, lambda i: dvl.draft_topk(hs[i % R4], hh, 4, ids=ids,
+                                                             logits=lg, ws=ws), 50, R)
+            out[f"c4_union53k_M{M}_top4"] = entry(RL.call_bytes(wl4.N, wl4.K, M, k=4), *t, peak,
+                                                  {"l2_rotation_copies": R4})
         del hs, W
     # NVFP4 trimmed head
     wl5 = S.c5()

@@ -1,4 +1,4 @@
-// Fused skinny projection + argmax on the tensor cores (tcgen05, TMEM) for
+// Fused skinny projection + argmax / top-k on the tensor cores (tcgen05, TMEM) for
 // batched drafting: 5 to 32 hidden rows at once ("[DGX Spark]
 // Qwen3.8-Flash-Next on two DGX Sparks", section "Five changes in 16 days":
 // MTP with 4 draft slots, 8 concurrent streams; "Shortlist MTP", section
@@ -20,7 +20,9 @@
 //   warp 2   allocates and frees the TMEM columns;
 //   warps 4-7 epilogue: each reads its 32-lane quadrant of the finished
 //            accumulator (tcgen05.ld), forms the packed (logit, full id) key
-//            of every row and keeps the best per hidden row.
+//            of every row and keeps the best per hidden row (argmax), or -
+//            for top-k - passes the keys through shared memory so that lane
+//            m folds hidden row m's 32 keys of the tile into its own list.
 // The block's best keys then go through the same cross-block finish as the
 // CUDA-core kernels.  Every mbarrier wait is bounded (about 2 s); on a
 // timeout the block records DVL_ERR_TIMEOUT, stops, waits (bounded) for its
@@ -49,7 +51,7 @@ constexpr int kEpiWarp0 = 4;           // warps 4..7: TMEM lane quadrants 0..3
 
 constexpr int kBoxes = 2;              // 64-wide k boxes per pipeline stage
 
-template <int NM>
+template <int NM, int KM>
 struct TcLayout {
     static constexpr int kHTile = NM * kBK * 2;
     static constexpr int kWStage = kBoxes * kWTile;
@@ -63,7 +65,11 @@ struct TcLayout {
     static constexpr size_t misc_off = bar_off + (size_t)(2 * kStages + 5) * 8;
     // tmem base, abort flag, issued, consumed
     static constexpr size_t cand_off = misc_off + 16;
-    static constexpr size_t bytes = cand_off + (size_t)DVL_MAX_M * 4 * 8;
+    // top-k: per epilogue warp, its 32 rows' keys for every hidden row
+    // [32][NM + 1] (one pad key per row spreads a column over the banks)
+    static constexpr size_t keys_off = cand_off + (size_t)DVL_MAX_M * 4 * KM * 8;
+    static constexpr size_t kKeyRow = NM + 1;
+    static constexpr size_t bytes = keys_off + (KM > 1 ? (size_t)4 * 32 * kKeyRow * 8 : 0);
     static constexpr size_t dyn_bytes = bytes + 1024;  // room to align the base to 1 KB
 };
 
@@ -95,12 +101,12 @@ __device__ __noinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
     }
 }
 
-template <int NM>
+template <int NM, int KM>
 __global__ void __launch_bounds__(kThreads, 1)
     argmax_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const __grid_constant__ CUtensorMap tmap_h, const ArgmaxArgs a, const int M)
 {
-    using L = TcLayout<NM>;
+    using L = TcLayout<NM, KM>;
     constexpr int S = L::kStages;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -113,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *drain = tempty + 2;
     // misc[0] TMEM base, [1] abort flag, [2] stages issued, [3] stages consumed
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + L::misc_off);
-    uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + L::cand_off);  // [M][4]
+    uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + L::cand_off);  // [M][4][KM]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KC = a.K / kBK;
@@ -219,10 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= kEpiWarp0) {
         // ---- epilogue: TMEM quadrant q holds rows q*32 .. q*32+31 ----
         const int q = warp - kEpiWarp0;
-        uint64_t best[NM];
+        uint64_t best[KM == 1 ? NM : 1];  // argmax: the best key per hidden row
 #pragma unroll
-        for (int m = 0; m < NM; ++m)
+        for (int m = 0; m < (KM == 1 ? NM : 1); ++m)
             best[m] = 0ull;
+        TopList<KM> mine;  // top-k: lane m keeps hidden row m's list
+        mine.init();
         pdl_wait();
         for (int t = 0; t < ntiles; ++t) {
             const int b = t & 1;
@@ -242,24 +250,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0)
                 mbar_arrive(&tempty[b]);
             const int row = r0 + t * kBM + q * 32 + lane;
-            if (row < r1) {
-                const int id = a.d2t ? __ldg(a.d2t + row) : (int)(a.id_base + row);
+            const bool in = row < r1;
+            const int id = in ? (a.d2t ? __ldg(a.d2t + row) : (int)(a.id_base + row)) : 0;
+            if constexpr (KM == 1) {
+                if (in) {
 #pragma unroll
-                for (int m = 0; m < NM; ++m) {
-                    if (m < M) {
-                        const uint64_t key = make_key(__uint_as_float(v[m]), id);
-                        best[m] = key > best[m] ? key : best[m];
+                    for (int m = 0; m < NM; ++m) {
+                        if (m < M) {
+                            const uint64_t key = make_key(__uint_as_float(v[m]), id);
+                            best[m] = key > best[m] ? key : best[m];
+                        }
                     }
                 }
+            } else {
+                // transpose through shared memory: each lane writes its row's
+                // keys, then lane m folds hidden row m's 32 keys into its list
+                uint64_t *sk = reinterpret_cast<uint64_t *>(smem + L::keys_off) +
+                               (size_t)q * 32 * L::kKeyRow;
+#pragma unroll
+                for (int m = 0; m < NM; ++m)
+                    if (m < M)
+                        sk[lane * L::kKeyRow + m] = in ? make_key(__uint_as_float(v[m]), id) : 0ull;
+                __syncwarp();
+                if (lane < M) {
+                    // most keys lose to the list's last entry: one compare each
+#pragma unroll 4
+                    for (int r = 0; r < 32; ++r) {
+                        const uint64_t key = sk[r * L::kKeyRow + lane];
+                        if (key > mine.v[KM - 1])
+                            mine.insert(key);
+                    }
+                }
+                __syncwarp();
             }
         }
+        if constexpr (KM == 1) {
 #pragma unroll
-        for (int m = 0; m < NM; ++m) {
-            if (m < M) {
-                const uint64_t k = warp_max_u64(best[m]);
-                if (lane == 0)
-                    s_cand[m * 4 + q] = k;
+            for (int m = 0; m < NM; ++m) {
+                if (m < M) {
+                    const uint64_t k = warp_max_u64(best[m]);
+                    if (lane == 0)
+                        s_cand[m * 4 + q] = k;
+                }
             }
+        } else if (lane < M) {
+#pragma unroll
+            for (int i = 0; i < KM; ++i)
+                s_cand[(lane * 4 + q) * KM + i] = mine.v[i];
         }
     }
     __syncthreads();
@@ -273,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_thread_sync();
     if (warp == 2)
         tc::tmem_dealloc(tmem_base, L::kTmemCols);
-    block_finish<1>(s_cand, M, 4, a);
+    block_finish<KM>(s_cand, M, 4, a);
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
@@ -310,10 +347,10 @@ bool encode_bf16_2d(CUtensorMap *m, const void *base, int K, int rows, int box_r
            CUDA_SUCCESS;
 }
 
-template <int NM>
+template <int NM, int KM>
 cudaError_t launch_nm(const ArgmaxArgs &a, int M, cudaStream_t s)
 {
-    using L = TcLayout<NM>;
+    using L = TcLayout<NM, KM>;
     alignas(64) CUtensorMap tw, th;
     std::memset(&tw, 0, sizeof tw);
     std::memset(&th, 0, sizeof th);
@@ -323,7 +360,7 @@ cudaError_t launch_nm(const ArgmaxArgs &a, int M, cudaStream_t s)
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess)
         return e;
-    auto kern = argmax_tc_kernel<NM>;
+    auto kern = argmax_tc_kernel<NM, KM>;
     int per_sm = 0;
     e = blocks_per_sm(reinterpret_cast<const void *>(kern), kThreads, L::dyn_bytes, &per_sm);
     if (e != cudaSuccess)
@@ -346,9 +383,11 @@ cudaError_t launch_nm(const ArgmaxArgs &a, int M, cudaStream_t s)
 
 bool tc_argmax_supported(int M, int K) { return M > 4 && M <= 32 && K % kBK == 0; }
 
-cudaError_t launch_argmax_tc(const ArgmaxArgs &a, int M, cudaStream_t s)
+cudaError_t launch_argmax_tc(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s)
 {
-    return M <= 16 ? launch_nm<16>(a, M, s) : launch_nm<32>(a, M, s);
+    if (kmax == 1)
+        return M <= 16 ? launch_nm<16, 1>(a, M, s) : launch_nm<32, 1>(a, M, s);
+    return M <= 16 ? launch_nm<16, 4>(a, M, s) : launch_nm<32, 4>(a, M, s);
 }
 
 }  // namespace dvl

@@ -159,16 +159,16 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
     a.k = k;
     a.ws = static_cast<unsigned char *>(ws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (hd->dtype == DVL_BF16 && k == 1 && tc_argmax_supported(M, hd->K)) {
+    const int kmax = k == 1 ? 1 : DVL_MAX_TOPK;
+    if (hd->dtype == DVL_BF16 && tc_argmax_supported(M, hd->K)) {
         // 5..32 rows: one pass on the tensor cores instead of several
         // CUDA-core passes over the head
         a.h = static_cast<const uint16_t *>(h);
         a.ids = ids;
         a.logits = logits;
-        cudaError_t e = launch_argmax_tc(a, M, s);
+        cudaError_t e = launch_argmax_tc(a, M, kmax, s);
         return e == cudaSuccess ? DVL_OK : cuda_failed(e);
     }
-    const int kmax = k == 1 ? 1 : DVL_MAX_TOPK;
     for (int m0 = 0; m0 < M; m0 += chunk) {
         const int mc = M - m0 < chunk ? M - m0 : chunk;
         a.h = static_cast<const uint16_t *>(h) + (size_t)m0 * hd->K;

@@ -108,12 +108,16 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t x)
 // lane swaps lists with its partner; the elementwise maximum of one
 // descending list and the other reversed holds the KM largest keys of both
 // as a bitonic sequence, which a bitonic merge network puts in order.
+// `width` (a power of two <= 32) limits the merge to aligned groups of that
+// many lanes; each group ends with its own best keys.
 template <int KM>
-__device__ __forceinline__ void warp_merge_topk(TopList<KM> &L)
+__device__ __forceinline__ void warp_merge_topk(TopList<KM> &L, int width = 32)
 {
     static_assert((KM & (KM - 1)) == 0, "KM must be a power of two");
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
+        if (off >= width)
+            continue;
         uint64_t o[KM];
 #pragma unroll
         for (int i = 0; i < KM; ++i)
@@ -166,12 +170,13 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[P])
 
 // Cross-block finish of a reducing kernel.  Every block calls it once, after
 // its own candidates are final, with s_cand holding, for each of the M rows,
-// `nlists` lists of KM keys ([M][nlists][KM] in shared memory; nlists is a
-// multiple of 32, lane l of the merging warp takes lists l, l + 32, ...).
+// `nlists` lists of KM keys ([M][nlists][KM] in shared memory; lane l of
+// the merging warp takes lists l, l + 32, ...).
 //  - k == 1: the block's best key per row goes to the workspace with a 64-bit
 //    atomicMax; the last block to finish swaps each key back to 0 and writes
 //    the id and the logit.
-//  - k > 1: the block's k best keys per row go to its own workspace slots;
+//  - k > 1: the block's k best keys per row go to its own workspace slots
+//    ([M][blocks][k]);
 //    the last block merges every block's slots.
 // The last block is found with a wrapping ticket (atomicInc up to
 // gridDim.x - 1), so the ticket is 0 again when the call ends.  No block
@@ -204,7 +209,7 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
 #pragma unroll
             for (int i = 0; i < KM; ++i)
                 if (lane == i)
-                    slots[((size_t)blockIdx.x * M + m) * KM + i] = L.v[i];
+                    slots[((size_t)m * gridDim.x + blockIdx.x) * KM + i] = L.v[i];
         }
     }
     __threadfence();  // this thread's slot stores before the ticket
@@ -225,57 +230,89 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
             a.logits[m] = key_logit(key);
         }
     } else {
-        // Every warp takes part: warp w merges row w % M over a share of the
-        // blocks, its lanes loading kBatch blocks' slots before inserting any
-        // (one L2 round trip per batch rather than per block); then one warp
-        // per row merges the warps' lists (at most 32 of them, one per lane).
-        // The reducing kernels have M <= nwarps whenever k > 1.
-        constexpr int kBatch = 4;
-        constexpr int kFinWarps = 32;  // the most warps a block can have
-        __shared__ uint64_t s_fin[kFinWarps][KM];
-        const int wpm = nwarps / M;  // warps per hidden row
-        const int m = warp % M, q = warp / M;
-        TopList<KM> L;
-        L.init();
-        if (q < wpm) {
-            const int stride = 32 * wpm;
-            for (int c0 = 32 * q + lane; c0 < (int)gridDim.x; c0 += kBatch * stride) {
-                uint64_t v[kBatch][KM];
+        // The slots are [M][blocks][KM]: one hidden row's lists are
+        // contiguous, so a warp's lanes read consecutive lists, 16 bytes at
+        // a time, kBatch blocks each before inserting any (one L2 round
+        // trip per batch).
+        static_assert(KM % 2 == 0, "lists are read in pairs of keys");
+        constexpr int kBatch = 8;
+        const int G = (int)gridDim.x;
+        auto gather = [&](TopList<KM> &L, int m, int c_first, int c_step) {
+            const uint64_t *row = reinterpret_cast<const uint64_t *>(slots) + (size_t)m * G * KM;
+            for (int c0 = c_first; c0 < G; c0 += kBatch * c_step) {
+                ulonglong2 v[kBatch][KM / 2];
 #pragma unroll
                 for (int u = 0; u < kBatch; ++u) {
-                    const int c = c0 + u * stride;
+                    const int c = c0 + u * c_step;
 #pragma unroll
-                    for (int i = 0; i < KM; ++i)
-                        v[u][i] = c < (int)gridDim.x ? __ldcg(slots + ((size_t)c * M + m) * KM + i)
-                                                     : 0ull;
+                    for (int i = 0; i < KM / 2; ++i)
+                        v[u][i] = c < G ? __ldcg(reinterpret_cast<const ulonglong2 *>(
+                                              row + (size_t)c * KM) + i)
+                                        : make_ulonglong2(0ull, 0ull);
                 }
 #pragma unroll
                 for (int u = 0; u < kBatch; ++u)
 #pragma unroll
-                    for (int i = 0; i < KM; ++i)
-                        L.insert(v[u][i]);
+                    for (int i = 0; i < KM / 2; ++i) {
+                        L.insert(v[u][i].x);
+                        L.insert(v[u][i].y);
+                    }
             }
-        }
-        warp_merge_topk<KM>(L);
-        if (lane == 0 && warp < kFinWarps) {
-#pragma unroll
-            for (int i = 0; i < KM; ++i)
-                s_fin[warp][i] = q < wpm ? L.v[i] : 0ull;
-        }
-        __syncthreads();
-        if (warp < M) {
-            TopList<KM> F;  // the warps' lists are already in order
-#pragma unroll
-            for (int i = 0; i < KM; ++i)
-                F.v[i] = lane < wpm ? s_fin[warp + M * lane][i] : 0ull;
-            warp_merge_topk<KM>(F);
+        };
+        auto write_row = [&](const TopList<KM> &F, int m) {
             if (lane < a.k && lane < KM) {
                 uint64_t key = F.v[0];
 #pragma unroll
                 for (int i = 1; i < KM; ++i)
                     key = lane == i ? F.v[i] : key;
-                a.ids[warp * a.k + lane] = key_id(key);
-                a.logits[warp * a.k + lane] = key_logit(key);
+                a.ids[m * a.k + lane] = key_id(key);
+                a.logits[m * a.k + lane] = key_logit(key);
+            }
+        };
+        if (M >= nwarps) {
+            // tpr threads per hidden row (a power of two, at most a warp),
+            // every row in one pass, no block-wide step
+            int tpr = 32;
+            while (tpr * M > (int)blockDim.x)
+                tpr >>= 1;
+            const int m = threadIdx.x / tpr, sub = threadIdx.x % tpr;
+            TopList<KM> L;
+            L.init();
+            if (m < M)
+                gather(L, m, sub, tpr);
+            warp_merge_topk<KM>(L, tpr);
+            if (m < M && sub < a.k && sub < KM) {
+                uint64_t key = L.v[0];
+#pragma unroll
+                for (int i = 1; i < KM; ++i)
+                    key = sub == i ? L.v[i] : key;
+                a.ids[m * a.k + sub] = key_id(key);
+                a.logits[m * a.k + sub] = key_logit(key);
+            }
+        } else {
+            // nwarps / M warps per hidden row, merged through shared memory
+            constexpr int kFinWarps = 32;  // the most warps a block can have
+            __shared__ uint64_t s_fin[kFinWarps][KM];
+            const int wpm = nwarps / M;
+            const int m = warp % M, q = warp / M;
+            TopList<KM> L;
+            L.init();
+            if (q < wpm)
+                gather(L, m, 32 * q + lane, 32 * wpm);
+            warp_merge_topk<KM>(L);
+            if (lane == 0) {
+#pragma unroll
+                for (int i = 0; i < KM; ++i)
+                    s_fin[warp][i] = q < wpm ? L.v[i] : 0ull;
+            }
+            __syncthreads();
+            if (warp < M) {
+                TopList<KM> F;  // the warps' lists are already in order
+#pragma unroll
+                for (int i = 0; i < KM; ++i)
+                    F.v[i] = lane < wpm ? s_fin[warp + M * lane][i] : 0ull;
+                warp_merge_topk<KM>(F);
+                write_row(F, warp);
             }
         }
     }

@@ -56,9 +56,10 @@ cudaError_t launch_argmax_bf16(const ArgmaxArgs &a, int M, int kmax, cudaStream_
 cudaError_t launch_argmax_lowbit(const ArgmaxArgs &a, int dtype, int M, int kmax,
                                  cudaStream_t s);
 int max_chunk_rows_bf16(int K);
-// Tensor-core argmax (bf16, k = 1) for 5..32 hidden rows in one launch.
+// Tensor-core argmax / top-k (bf16; kmax 1 or 4) for 5..32 hidden rows in
+// one launch.
 bool tc_argmax_supported(int M, int K);
-cudaError_t launch_argmax_tc(const ArgmaxArgs &a, int M, cudaStream_t s);
+cudaError_t launch_argmax_tc(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
 int max_chunk_rows_lowbit(int K);
 
 // The argument checks of draft_argmax / draft_topk, without the workspace.

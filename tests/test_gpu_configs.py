@@ -7,7 +7,8 @@ c2  the full 248,320 x 2,560 head, M in {1, 3}, argmax and top-4; candidate
     scores of 16 hidden rows x 32 candidates through it
 c3  32,768-row FR-Spec trim of a 248,320 x 5,120 head, ranks built on the
     host from a Zipf token stream, M in {1, 2, 3, 4}
-c4  52,755-row union list, M in {8, 16, 32}, planted near-ties
+c4  52,755-row union list, M in {8, 16, 32}, planted near-ties, argmax and
+    top-4
 c5  NVFP4 32,768 x 5,120 head with a rank-order d2t, M in {1, 3}
 """
 import numpy as np
@@ -142,6 +143,10 @@ def test_c4_batched_near_ties(dvl, oracle_mod):
         report(f"c4 M={M}", rep)
         exempt_total += rep["rows_exempt"]
         exact_total += rep["rows_exact"]
+        # batched top-4 in the same single pass over the head
+        ids, vals = dvl.draft_topk(head, dev(h), 4, ws=dvl.make_workspace(M, 4))
+        report(f"c4 M={M} top4", check_topk(oracle_mod, L, wl.d2t, 4, ids.cpu().numpy(),
+                                              vals.cpu().numpy()))
     assert exempt_total > 0 and exact_total > 0
 
 
