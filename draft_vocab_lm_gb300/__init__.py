@@ -119,6 +119,7 @@ class Head:
     def struct(self) -> DvlHead:
         if self._struct is None:
             self._struct = self._make_struct()
+        self._struct.flags = DVL_HEAD_STATIC if self.static else 0  # static may change
         return self._struct
 
     def _make_struct(self) -> DvlHead:

@@ -1,6 +1,8 @@
 // The C ABI: argument checks, workspace handling, dispatch to the kernels.
-// Every check runs on the host before anything is enqueued; nothing here
-// allocates, frees or synchronizes.
+// Every check runs on the host before anything is enqueued.  Nothing here
+// allocates or frees device memory, and nothing synchronizes except the two
+// calls that read a word back to the host: dvl_quantize_head (the head's
+// maximum, at load time) and dvl_workspace_status.
 #include <cuda_runtime.h>
 
 #include <cstdint>
