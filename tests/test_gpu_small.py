@@ -278,3 +278,55 @@ def test_workspace_status_reads_and_clears(dvl, oracle_mod):
         ids, _ = dvl.draft_argmax(head, dev(h), ws=ws)
         assert np.array_equal(ids.cpu().numpy(), oracle_mod.argmax(L)[0])
     assert dvl.workspace_status(ws) == 0
+
+
+def test_two_streams_with_their_own_workspaces(dvl, oracle_mod):
+    # calls interleaved on two streams, each with its own workspace (the
+    # documented rule for concurrent calls): CUDA-core, tensor-core and
+    # low-bit kernels, argmax and top-k, all as the oracle says
+    rng = np.random.default_rng(33)
+    N, K = 6000, 256
+    w = int_bf16(rng, (N, K))
+    head = dvl.Head(dev(w))
+    q, sc, g = S.quantize_nvfp4(S.normal_bf16_rows(34, N, K, 0.02))
+    head4 = dvl.Head(dev(q), scales=dev(sc), global_scale=g)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    wss = [dvl.make_workspace(32, 4), dvl.make_workspace(32, 4)]
+    torch.cuda.synchronize()
+    inputs = []
+    for it in range(12):
+        M = [1, 3, 8, 20][it % 4]
+        h = int_bf16(rng, (M, K))
+        inputs.append((it, h, dev(h)))
+    torch.cuda.synchronize()  # every input in place; the launches below overlap
+    jobs = []
+    for it, h, hd in inputs:
+        sidx = it % 2
+        k = 1 if it % 3 else 4
+        hh = head4 if it % 5 == 4 else head
+        with torch.cuda.stream(streams[sidx]):
+            ids = torch.empty((h.shape[0], k), dtype=torch.int32, device="cuda")
+            vals = torch.empty((h.shape[0], k), dtype=torch.float32, device="cuda")
+            if k == 1:
+                dvl.draft_argmax(hh, hd, ids=ids.view(-1), logits=vals.view(-1), ws=wss[sidx],
+                                 stream=streams[sidx])
+            else:
+                dvl.draft_topk(hh, hd, k, ids=ids, logits=vals, ws=wss[sidx], stream=streams[sidx])
+        jobs.append((hh is head4, h, k, (ids, vals)))
+    torch.cuda.synchronize()
+    from parity import check_argmax, check_topk
+    for is4, h, k, (ids, vals) in jobs:
+        if is4:
+            L, _ = oracle_mod.logits_nvfp4(q, sc, g, h)
+            if k == 1:
+                check_argmax(oracle_mod, L, None, ids.cpu().numpy().ravel(),
+                             vals.cpu().numpy().ravel())
+            else:
+                check_topk(oracle_mod, L, None, k, ids.cpu().numpy(), vals.cpu().numpy())
+        else:
+            L, _ = oracle_mod.logits_bf16(w, h)
+            o_ids, o_vals, _ = oracle_mod.topk(L, k)
+            got = ids.cpu().numpy().reshape(o_ids.shape)
+            assert np.array_equal(got, o_ids)
+    for ws in wss:
+        assert dvl.workspace_status(ws) == 0
