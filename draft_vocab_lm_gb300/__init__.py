@@ -27,7 +27,8 @@ from ._native import (DVL_BF16, DVL_FP8, DVL_HEAD_STATIC, DVL_K_MULTIPLE, DVL_MA
                       DVL_MAX_TOPK, DVL_NVFP4, DvlError, DvlHead, check, lib)
 
 __all__ = [
-    "Head", "DvlError", "workspace_status", "draft_argmax", "draft_topk", "score_ids", "trim_head", "learn_rows",
+    "Head", "DvlError", "workspace_status", "draft_argmax", "draft_topk", "draft_plan", "score_ids", "trim_head",
+    "learn_rows",
     "quantize_head",
     "Shortlist", "workspace_bytes",
     "make_workspace", "workspace_init", "histogram", "build_ranks", "union_sorted",
@@ -224,6 +225,17 @@ def draft_argmax(head: Head, h, *, ids=None, logits=None, ws=None, stream=None):
                                  logits.data_ptr(), ws.data_ptr(), ws.numel(),
                                  _stream_handle(stream, h.device)))
     return ids, logits
+
+
+def draft_plan(head: Head, M: int, k: int = 1):
+    """(kernel family, launches) of a draft_argmax (k = 1) / draft_topk call
+    with this head and M hidden rows on the current device; launches
+    nothing."""
+    name = ctypes.c_char_p()
+    n = ctypes.c_int32()
+    check("dvl_draft_plan", lib().dvl_draft_plan(ctypes.byref(head.struct()), int(M), int(k),
+                                                 ctypes.byref(name), ctypes.byref(n)))
+    return name.value.decode(), n.value
 
 
 def score_ids(head: Head, h, ids, *, logits=None, stream=None):

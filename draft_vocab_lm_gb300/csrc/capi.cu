@@ -317,6 +317,48 @@ dvl_status dvl_draft_topk(const dvl_head *head, const void *h, int32_t M, int32_
     return reduce_call(head, h, M, k, ids, logits, ws, ws_bytes, stream);
 }
 
+dvl_status dvl_draft_plan(const dvl_head *head, int32_t M, int32_t k, const char **kernel,
+                          int32_t *launches)
+{
+    dvl_status st = check_head(head);
+    if (st != DVL_OK)
+        return st;
+    if (M < 1 || M > DVL_MAX_M || k < 1 || k > DVL_MAX_TOPK || k > head->N || !kernel ||
+        !launches)
+        return DVL_ERR_INVALID_ARG;
+    if (head->dtype != DVL_BF16) {
+        const int chunk = max_chunk_rows_lowbit(head->K);
+        if (chunk < 1)
+            return DVL_ERR_UNSUPPORTED;
+        *kernel = head->dtype == DVL_NVFP4 ? "nvfp4-mma" : "fp8-mma";
+        *launches = (M + chunk - 1) / chunk;
+        return DVL_OK;
+    }
+    if (tc_argmax_supported(M, head->K)) {
+        *kernel = "bf16-tcgen05";
+        *launches = 1;
+        return DVL_OK;
+    }
+    const int chunk = max_chunk_rows_bf16(head->K);
+    if (chunk < 1)
+        return DVL_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    const cudaError_t e = device_info(&di);
+    if (e != cudaSuccess)
+        return cuda_failed(e);
+    bool mma = false, cores = false;
+    for (int m0 = 0; m0 < M; m0 += chunk) {
+        const int mc = M - m0 < chunk ? M - m0 : chunk;
+        if (bf16_uses_mma(head->w, head->N, head->K, mc, di.sms))
+            mma = true;
+        else
+            cores = true;
+    }
+    *kernel = mma ? (cores ? "bf16-mma+cuda-cores" : "bf16-mma") : "bf16-cuda-cores";
+    *launches = (M + chunk - 1) / chunk;
+    return DVL_OK;
+}
+
 dvl_status dvl_score_ids(const dvl_head *head, const void *h, int32_t M, const int32_t *ids,
                          int32_t c, float *logits, void *stream)
 {

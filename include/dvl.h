@@ -183,6 +183,24 @@ dvl_status dvl_draft_topk(const dvl_head *head, const void *h, int32_t M, int32_
                           int32_t *ids, float *logits, void *ws, size_t ws_bytes,
                           void *stream);
 
+/* Which kernels a dvl_draft_argmax (k = 1) or dvl_draft_topk call with this
+ * head, M and k launches, for logs and tests; enqueues nothing.  *kernel is
+ * a static string owned by the library:
+ *   "bf16-cuda-cores"  CUDA-core kernel (one or two hidden rows, widths
+ *                      other than 2,560 / 5,120, short heads);
+ *   "bf16-mma"         register-path tensor cores (three or four hidden
+ *                      rows, width 2,560 or 5,120, a 32-byte aligned head of
+ *                      at least 8 rows per warp of the grid);
+ *   "bf16-mma+cuda-cores"  chunks of both kinds;
+ *   "bf16-tcgen05"     5th-generation tensor cores (5 .. 32 hidden rows);
+ *   "nvfp4-mma", "fp8-mma"  the low-bit heads.
+ * *launches is the number of kernel launches of the call.  The choice
+ * depends on the current device's SM count.
+ * Errors: those of dvl_draft_topk's head and M / k checks, and
+ * DVL_ERR_CUDA when the device cannot be queried. */
+dvl_status dvl_draft_plan(const dvl_head *head, int32_t M, int32_t k, const char **kernel,
+                          int32_t *launches);
+
 /* dvl_draft_argmax for callers that cannot allocate device memory.  The
  * pages have no counterpart of this entry point.
  *

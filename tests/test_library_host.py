@@ -229,3 +229,23 @@ def test_quantize_checks_reject_before_any_launch(dvl):
     assert L.dvl_quantize_head(ctypes.byref(h), DVL_NVFP4, 0x1000, 0x2000, None, ok_ws, 512, None) == 1
     assert L.dvl_quantize_head(ctypes.byref(h), DVL_FP8, 0x1000, None, ctypes.byref(g), None, 512, None) == 4
     assert L.dvl_quantize_head(ctypes.byref(h), DVL_FP8, 0x1000, None, ctypes.byref(g), ok_ws, 100, None) == 4
+
+
+def test_plan_without_a_device(dvl):
+    # argument checks first; low-bit and 5+-row bf16 plans need no device
+    from draft_vocab_lm_gb300._native import lib, DVL_FP8, DVL_NVFP4
+    L = lib()
+    name, n = ctypes.c_char_p(), ctypes.c_int32()
+    h = _head()
+    assert L.dvl_draft_plan(ctypes.byref(h), 0, 1, ctypes.byref(name), ctypes.byref(n)) == 1
+    assert L.dvl_draft_plan(ctypes.byref(h), 1, 5, ctypes.byref(name), ctypes.byref(n)) == 1
+    assert L.dvl_draft_plan(ctypes.byref(h), 1, 1, None, ctypes.byref(n)) == 1
+    assert L.dvl_draft_plan(ctypes.byref(_head(K=100)), 1, 1, ctypes.byref(name), ctypes.byref(n)) == 1
+    assert L.dvl_draft_plan(ctypes.byref(h), 5, 4, ctypes.byref(name), ctypes.byref(n)) == 0
+    assert (name.value, n.value) == (b"bf16-tcgen05", 1)
+    assert L.dvl_draft_plan(ctypes.byref(_head(dtype=DVL_FP8)), 3, 1, ctypes.byref(name),
+                            ctypes.byref(n)) == 0
+    assert (name.value, n.value) == (b"fp8-mma", 1)
+    nv = _head(dtype=DVL_NVFP4, scales=0x7000, K=5120)
+    assert L.dvl_draft_plan(ctypes.byref(nv), 32, 4, ctypes.byref(name), ctypes.byref(n)) == 0
+    assert name.value == b"nvfp4-mma" and n.value >= 4
