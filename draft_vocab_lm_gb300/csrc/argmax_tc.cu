@@ -49,14 +49,18 @@ constexpr int kBK = 64;                // k per stage (one 128-byte swizzle row)
 constexpr int kWTile = kBM * kBK * 2;  // 16 KB
 constexpr int kEpiWarp0 = 4;           // warps 4..7: TMEM lane quadrants 0..3
 
-constexpr int kBoxes = 2;              // 64-wide k boxes per pipeline stage
 
 template <int NM, int KM>
 struct TcLayout {
     static constexpr int kHTile = NM * kBK * 2;
+    // 64-wide k boxes per pipeline stage and stages in the ring, measured on
+    // GB300 (52,755-row head): three boxes x three stages for 16 hidden-row
+    // columns (1.3% faster than two x four), two x four for 32 (three boxes
+    // leave room for only two stages there: 8% slower).
+    static constexpr int kBoxes = NM == 32 ? 2 : 3;
     static constexpr int kWStage = kBoxes * kWTile;
     static constexpr int kHStage = kBoxes * kHTile;
-    static constexpr int kStages = (NM == 32 ? 8 : 9) / kBoxes;
+    static constexpr int kStages = NM == 32 ? 4 : 3;
     static constexpr int kTmemCols = 2 * NM < 32 ? 32 : 2 * NM;
     static constexpr size_t w_off = 0;
     static constexpr size_t h_off = w_off + (size_t)kStages * kWStage;
@@ -163,13 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < ntiles; ++t) {
                 const int row = r0 + t * kBM;
                 bool ok = true;
-                for (int kc = 0; kc < KC; kc += kBoxes, ++i) {
+                for (int kc = 0; kc < KC; kc += L::kBoxes, ++i) {
                     const int s = (int)(i % S);
                     if (!wait_or_abort(&empty[s], ((i / S) & 1u) ^ 1u, abort_flag, a.ws)) {
                         ok = false;
                         break;
                     }
-                    const int nb = min(kBoxes, KC - kc);
+                    const int nb = min(L::kBoxes, KC - kc);
                     mbar_arrive_expect_tx(&full[s], (uint32_t)(nb * (kWTile + L::kHTile)));
                     for (int bx = 0; bx < nb; ++bx) {
                         tc::tma_load_2d(sW + (size_t)s * L::kWStage + bx * kWTile, &tmap_w,
@@ -194,14 +198,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_after_thread_sync();
                 const uint32_t d = tmem_base + (uint32_t)(b * NM);
                 bool ok = true;
-                for (int kc = 0; kc < KC; kc += kBoxes, ++i) {
+                for (int kc = 0; kc < KC; kc += L::kBoxes, ++i) {
                     const int s = (int)(i % S);
                     if (!wait_or_abort(&full[s], (i / S) & 1u, abort_flag, a.ws)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_thread_sync();
-                    const int nb = min(kBoxes, KC - kc);
+                    const int nb = min(L::kBoxes, KC - kc);
                     for (int bx = 0; bx < nb; ++bx) {
                         const unsigned char *wt = sW + (size_t)s * L::kWStage + bx * kWTile;
                         const unsigned char *ht = sH + (size_t)s * L::kHStage + bx * L::kHTile;
