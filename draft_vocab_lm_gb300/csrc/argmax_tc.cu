@@ -54,13 +54,15 @@ template <int NM, int KM>
 struct TcLayout {
     static constexpr int kHTile = NM * kBK * 2;
     // 64-wide k boxes per pipeline stage and stages in the ring, measured on
-    // GB300 (52,755-row head): three boxes x three stages for 16 hidden-row
-    // columns (1.3% faster than two x four), two x four for 32 (three boxes
-    // leave room for only two stages there: 8% slower).
+    // GB300 (52,755-row head): three boxes per stage for 16 hidden-row
+    // columns (1.3% faster than two), two for 32 (three leave room for too
+    // few stages there: 8% slower).  Argmax has no key tile, and its shared
+    // memory takes one stage more (1.2-1.9% faster): 4 x 3 boxes for 16
+    // columns, 5 x 2 for 32; top-k keeps 3 x 3 and 4 x 2.
     static constexpr int kBoxes = NM == 32 ? 2 : 3;
     static constexpr int kWStage = kBoxes * kWTile;
     static constexpr int kHStage = kBoxes * kHTile;
-    static constexpr int kStages = NM == 32 ? 4 : 3;
+    static constexpr int kStages = NM == 32 ? (KM == 1 ? 5 : 4) : (KM == 1 ? 4 : 3);
     static constexpr int kTmemCols = 2 * NM < 32 ? 32 : 2 * NM;
     static constexpr size_t w_off = 0;
     static constexpr size_t h_off = w_off + (size_t)kStages * kWStage;
