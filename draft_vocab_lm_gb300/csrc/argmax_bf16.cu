@@ -17,13 +17,6 @@ int max_chunk_rows_bf16(int K)
     return r > 4 ? 4 : r;
 }
 
-bool bf16_uses_mma(const void *w, int N, int K, int M, int sms)
-{
-    return M >= 3 && M <= 4 && (K == 2560 || K == 5120) &&
-           (reinterpret_cast<uintptr_t>(w) & 31) == 0 &&
-           (long long)N >= (long long)bf16mma::kTile * bf16mma::kWarps * 2 * sms;
-}
-
 cudaError_t launch_argmax_bf16(const ArgmaxArgs &a_in, int M, int kmax, cudaStream_t s)
 {
     ArgmaxArgs a = a_in;

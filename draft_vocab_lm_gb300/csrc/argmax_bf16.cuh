@@ -29,7 +29,6 @@
 
 #include <cuda_runtime.h>
 
-#include "argmax_bf16_mma.cuh"
 #include "dvl_device.cuh"
 
 namespace dvl {
@@ -339,21 +338,8 @@ template <int M, int KM>
 cudaError_t launch_m(const ArgmaxArgs &a, cudaStream_t s)
 {
     static_assert(M <= 4, "5 or more hidden rows run on the tensor cores or in chunks");
-    // Three or four hidden rows on a head that gives every warp of the grid
-    // at least one full 8-row tile run on the register-path tensor cores
-    // (argmax_bf16_mma.cuh): there the CUDA cores' multiply-add issue, not
-    // HBM, sets the pace (measured on GB300: -1% on the full vocabulary,
-    // -3% on a 32,768 x 5,120 head).  One or two rows, and shorter heads,
-    // whose rows would stream through only 4 lanes each, stay here.
-    if constexpr (M >= 3) {
-        DeviceInfo di;
-        const cudaError_t e = device_info(&di);
-        if (e != cudaSuccess)
-            return e;
-        if (bf16_uses_mma(a.w, a.N, a.K, M, di.sms))
-            return a.K == 2560 ? bf16mma::launch<M, KM, 2560, 4>(a, s)
-                               : bf16mma::launch<M, KM, 5120, 4>(a, s);
-    }
+    // (Three to eight rows on a long head of width 2,560 or 5,120 never get
+    // here: the dispatch sends them to the register-path tensor cores.)
     // Ring depth NB (k steps in flight) and rows per group RPW, chosen by
     // measurement on GB300 among the variants that do not spill at 128
     // registers: a deep ring for M <= 2; for K = 5,120 and M = 3, 4 two rows

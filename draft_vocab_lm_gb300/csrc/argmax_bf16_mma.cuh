@@ -1,6 +1,6 @@
 // Fused skinny projection + argmax / top-k over a bf16 draft head, on the
 // register-path tensor cores, for the unrolled hidden widths (2,560 and
-// 5,120), three or four hidden rows and heads of at least one full 8-row
+// 5,120), three to eight hidden rows and heads of at least one full 8-row
 // tile per warp.  ("Shortlist MTP", sections "What I was
 // testing" and "What was actually happening": a hidden row of width 2,560
 // against every head row, M = 1 or 3 -- bandwidth-heavy, for a couple of
@@ -9,10 +9,11 @@
 // Why tensor cores for a memory-bound product: on CUDA cores every 16 bytes
 // of weights cost 8 widenings and 8 M fused multiply-adds, about 35 issued
 // instructions at M = 3, and the issue slots, not HBM, set the pace.  Here
-// every 32 bytes cost one load and four MMAs at any M <= 4.  The price is
-// that a row streams through 4 lanes instead of 32: a warp with a short
-// range spends more memory round trips on it, so one or two hidden rows
-// and heads of fewer rows stay on the CUDA cores.
+// every 32 bytes cost one load and four MMAs at any M <= 8 (and at 5 .. 8
+// rows it streams faster than the tcgen05 kernel's 128-row tiles).  The
+// price is that a row streams through 4 lanes instead of 32: a warp with a
+// short range spends more memory round trips on it, so one or two hidden
+// rows and heads of fewer rows stay on the CUDA cores.
 //
 // Operands of mma.sync m16n8k16 (bf16 in, fp32 accumulate):
 //   - B (16 k x 8 n) is 8 head rows: lane (g, q) = (lane / 4, lane % 4)
@@ -57,6 +58,7 @@ constexpr int kTile = 8;        // head rows per MMA tile (MMA n)
 constexpr int kChunk = 128;     // weights per row per k chunk (2 loads per lane)
 constexpr int kLists = kWarps * 4;  // per hidden row per block: lanes (g = m, q < 4) of each warp
 constexpr int kAcc = 4;         // independent accumulators (MMA dependency chains)
+constexpr int kMaxRows = 8;     // hidden rows per launch (rows of the A operand in use)
 
 // D += A B for one m16n8k16 MMA whose A rows 8..15 are zero.
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0,
@@ -96,7 +98,7 @@ __host__ __device__ constexpr size_t smem_bytes()
 template <int M, int KM, int KC, int NB>
 __global__ void __launch_bounds__(kThreads, 2) argmax_mma_kernel(const ArgmaxArgs a)
 {
-    static_assert(M >= 1 && M <= 4, "one to four hidden rows");
+    static_assert(M >= 1 && M <= kMaxRows, "one to eight hidden rows");
     static_assert(KC % kChunk == 0, "the width must be a multiple of the chunk");
     constexpr int CC = KC / kChunk;
     static_assert(CC % NB == 0, "the ring must divide the chunks");

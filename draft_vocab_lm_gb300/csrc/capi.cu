@@ -162,6 +162,21 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
     a.ws = static_cast<unsigned char *>(ws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int kmax = k == 1 ? 1 : DVL_MAX_TOPK;
+    if (hd->dtype == DVL_BF16 && M >= 3) {
+        DeviceInfo di;
+        const cudaError_t e = device_info(&di);
+        if (e != cudaSuccess)
+            return cuda_failed(e);
+        if (bf16_uses_mma(hd->w, hd->N, hd->K, M, di.sms)) {
+            // 3..8 rows on a long head: one pass on the register-path tensor
+            // cores
+            a.h = static_cast<const uint16_t *>(h);
+            a.ids = ids;
+            a.logits = logits;
+            const cudaError_t el = launch_argmax_bf16_mma(a, M, kmax, s);
+            return el == cudaSuccess ? DVL_OK : cuda_failed(el);
+        }
+    }
     if (hd->dtype == DVL_BF16 && tc_argmax_supported(M, hd->K)) {
         // 5..32 rows: one pass on the tensor cores instead of several
         // CUDA-core passes over the head
@@ -334,6 +349,17 @@ dvl_status dvl_draft_plan(const dvl_head *head, int32_t M, int32_t k, const char
         *launches = (M + chunk - 1) / chunk;
         return DVL_OK;
     }
+    if (M >= 3) {
+        DeviceInfo di;
+        const cudaError_t e = device_info(&di);
+        if (e != cudaSuccess)
+            return cuda_failed(e);
+        if (bf16_uses_mma(head->w, head->N, head->K, M, di.sms)) {
+            *kernel = "bf16-mma";
+            *launches = 1;
+            return DVL_OK;
+        }
+    }
     if (tc_argmax_supported(M, head->K)) {
         *kernel = "bf16-tcgen05";
         *launches = 1;
@@ -342,19 +368,7 @@ dvl_status dvl_draft_plan(const dvl_head *head, int32_t M, int32_t k, const char
     const int chunk = max_chunk_rows_bf16(head->K);
     if (chunk < 1)
         return DVL_ERR_UNSUPPORTED;
-    DeviceInfo di;
-    const cudaError_t e = device_info(&di);
-    if (e != cudaSuccess)
-        return cuda_failed(e);
-    bool mma = false, cores = false;
-    for (int m0 = 0; m0 < M; m0 += chunk) {
-        const int mc = M - m0 < chunk ? M - m0 : chunk;
-        if (bf16_uses_mma(head->w, head->N, head->K, mc, di.sms))
-            mma = true;
-        else
-            cores = true;
-    }
-    *kernel = mma ? (cores ? "bf16-mma+cuda-cores" : "bf16-mma") : "bf16-cuda-cores";
+    *kernel = "bf16-cuda-cores";
     *launches = (M + chunk - 1) / chunk;
     return DVL_OK;
 }

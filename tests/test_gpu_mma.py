@@ -1,5 +1,5 @@
 """GPU parity of the register-path tensor-core kernel for bf16 heads (three
-or four hidden rows, widths 2,560 and 5,120, heads of at least one full
+to eight hidden rows, widths 2,560 and 5,120, heads of at least one full
 8-row tile per warp), against the oracle: bit-exact argmax and top-4 on
 integer heads with a d2t map and with id_base, ragged tiles at the end of
 each warp's range, the same head one row short of the threshold (CUDA
@@ -48,7 +48,7 @@ def int_case(seed, N, K, M):
 
 
 @pytest.mark.parametrize("K", [2560, 5120])
-@pytest.mark.parametrize("M", [3, 4])
+@pytest.mark.parametrize("M", [3, 4, 5, 8])
 def test_mma_integer_head_bit_exact(dvl, oracle_mod, K, M):
     N = threshold_rows() + 555  # ragged: warps end on partial tiles
     rng, w, h = int_case(K + M, N, K, M)
@@ -109,13 +109,17 @@ def test_mma_and_cuda_core_paths_agree_and_dispatch(dvl, oracle_mod):
     assert dvl.draft_plan(head, 1) == ("bf16-cuda-cores", 1)
     assert dvl.draft_plan(head, 2, 4) == ("bf16-cuda-cores", 1)
     assert dvl.draft_plan(head, 4) == ("bf16-mma", 1)
-    assert dvl.draft_plan(head, 5) == ("bf16-tcgen05", 1)
+    assert dvl.draft_plan(head, 8, 4) == ("bf16-mma", 1)
+    assert dvl.draft_plan(head, 9) == ("bf16-tcgen05", 1)
     assert dvl.draft_plan(head, 32, 4) == ("bf16-tcgen05", 1)
+    short = dvl.Head(cases["short"][0])
+    assert dvl.draft_plan(short, 8) == ("bf16-tcgen05", 1)
     torch.cuda.synchronize()
     assert dvl.workspace_status(ws) == 0
 
 
-@pytest.mark.parametrize("N,K,M", [(20011, 2560, 3), (32768, 5120, 4), (40000, 2560, 4)])
+@pytest.mark.parametrize("N,K,M", [(20011, 2560, 3), (32768, 5120, 4), (40000, 2560, 4),
+                                   (52755, 2560, 8), (20011, 5120, 6)])
 def test_mma_gaussian_head_parity(dvl, oracle_mod, N, K, M):
     if N < threshold_rows():
         pytest.skip("head below the tensor-core threshold on this device")

@@ -232,7 +232,8 @@ def test_quantize_checks_reject_before_any_launch(dvl):
 
 
 def test_plan_without_a_device(dvl):
-    # argument checks first; low-bit and 5+-row bf16 plans need no device
+    # argument checks first; low-bit plans need no device; bf16 plans for
+    # three or more rows read the SM count (DVL_ERR_CUDA without a device)
     from draft_vocab_lm_gb300._native import lib, DVL_FP8, DVL_NVFP4
     L = lib()
     name, n = ctypes.c_char_p(), ctypes.c_int32()
@@ -241,8 +242,10 @@ def test_plan_without_a_device(dvl):
     assert L.dvl_draft_plan(ctypes.byref(h), 1, 5, ctypes.byref(name), ctypes.byref(n)) == 1
     assert L.dvl_draft_plan(ctypes.byref(h), 1, 1, None, ctypes.byref(n)) == 1
     assert L.dvl_draft_plan(ctypes.byref(_head(K=100)), 1, 1, ctypes.byref(name), ctypes.byref(n)) == 1
-    assert L.dvl_draft_plan(ctypes.byref(h), 5, 4, ctypes.byref(name), ctypes.byref(n)) == 0
-    assert (name.value, n.value) == (b"bf16-tcgen05", 1)
+    st = L.dvl_draft_plan(ctypes.byref(h), 5, 4, ctypes.byref(name), ctypes.byref(n))
+    assert st in (0, 5)
+    if st == 0:  # a 100-row head is below the register-path threshold
+        assert (name.value, n.value) == (b"bf16-tcgen05", 1)
     assert L.dvl_draft_plan(ctypes.byref(_head(dtype=DVL_FP8)), 3, 1, ctypes.byref(name),
                             ctypes.byref(n)) == 0
     assert (name.value, n.value) == (b"fp8-mma", 1)
