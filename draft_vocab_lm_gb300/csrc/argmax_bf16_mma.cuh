@@ -19,17 +19,17 @@
 //   - B (16 k x 8 n) is 8 head rows: lane (g, q) = (lane / 4, lane % 4)
 //     supplies column n = g, i.e. head row g of the tile, straight from the
 //     16-byte loads it issued (no conversion);
-//   - A (16 m x 16 k) is the hidden rows: lane (g, q) supplies row g (rows
-//     8..15 are zero); rows g >= M hold a copy of a valid row, and only feed
-//     result rows that nobody reads;
+//   - A (16 m x 16 k) is the hidden rows: lane (g, q) supplies rows g and
+//     g + 8 (rows 8..15 are zero when M <= 8); rows at or past M hold a copy
+//     of a valid row, and only feed result rows that nobody reads;
 //   - the k order inside an MMA is a permutation of the weights' k, the same
 //     for A and B: the k slots 2q, 2q + 1, 2q + 8, 2q + 9 of lane (g, q) are
 //     the weights kb .. kb + 3 with kb = 128 c + 64 w + 16 q + 4 s for chunk
 //     c, load w < 2 and quarter s < 4 of the lane's 32-byte load, so every
 //     product pairs the right weight and hidden value and every k is used
 //     once;
-//   - D lane (g, q) ends with the logits of hidden row g against head rows
-//     2q and 2q + 1 of the tile.
+//   - D lane (g, q) ends with the logits of hidden rows g and g + 8 against
+//     head rows 2q and 2q + 1 of the tile.
 //
 // Work split as in the CUDA-core kernel: a persistent grid of two 256-thread
 // blocks per SM, one balanced contiguous row range per warp, walked in tiles
@@ -58,16 +58,16 @@ constexpr int kTile = 8;        // head rows per MMA tile (MMA n)
 constexpr int kChunk = 128;     // weights per row per k chunk (2 loads per lane)
 constexpr int kLists = kWarps * 4;  // per hidden row per block: lanes (g = m, q < 4) of each warp
 constexpr int kAcc = 4;         // independent accumulators (MMA dependency chains)
-constexpr int kMaxRows = 8;     // hidden rows per launch (rows of the A operand in use)
+constexpr int kMaxRows = 16;    // hidden rows per launch (rows of the A operand)
 
-// D += A B for one m16n8k16 MMA whose A rows 8..15 are zero.
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0,
-                                         uint32_t b1)
+// D += A B for one m16n8k16 MMA: a0 / a2 hold A row g, a1 / a3 row g + 8.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
 {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // 32-byte load of weights read exactly once (no L1 allocation, 256-byte L2
@@ -98,7 +98,8 @@ __host__ __device__ constexpr size_t smem_bytes()
 template <int M, int KM, int KC, int NB>
 __global__ void __launch_bounds__(kThreads, 2) argmax_mma_kernel(const ArgmaxArgs a)
 {
-    static_assert(M >= 1 && M <= kMaxRows, "one to eight hidden rows");
+    static_assert(M >= 1 && M <= kMaxRows, "one to sixteen hidden rows");
+    constexpr bool kHi = M > 8;  // hidden rows 8.. fill the A operand's rows 8..15
     static_assert(KC % kChunk == 0, "the width must be a multiple of the chunk");
     constexpr int CC = KC / kChunk;
     static_assert(CC % NB == 0, "the ring must divide the chunks");
@@ -175,6 +176,10 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_mma_kernel(const ArgmaxArg
         acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     const bool hrow = g < M;
     const uint16_t *hp = s_h + (hrow ? g : M - 1) * P + 16 * q;
+    const bool hrow2 = kHi && g + 8 < M;  // this lane also ends with hidden row g + 8
+    const uint16_t *hp2 = s_h + (hrow2 ? g + 8 : M - 1) * P + 16 * q;
+    TopList<KM> best2;
+    best2.init();
 
     for (int t = 0; t < ntiles; ++t) {
         const bool vnext = (t + 1) * kTile + g < nrows;
@@ -191,15 +196,20 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_mma_kernel(const ArgmaxArg
         for (int c = 0; c < CC; ++c) {
             const int b = c % NB;
             // the hidden values of the same k as the lane's words
-            uint4 hv[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-                hv[w] = *reinterpret_cast<const uint4 *>(hp + kChunk * c + 64 * (w >> 1) +
-                                                         8 * (w & 1));
+            uint4 hv[4], hv2[4];
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                mma_bf16(acc[(2 * w) % kAcc], hv[w].x, hv[w].y, buf[b][w].x, buf[b][w].y);
-                mma_bf16(acc[(2 * w + 1) % kAcc], hv[w].z, hv[w].w, buf[b][w].z, buf[b][w].w);
+                const int off = kChunk * c + 64 * (w >> 1) + 8 * (w & 1);
+                hv[w] = *reinterpret_cast<const uint4 *>(hp + off);
+                hv2[w] = kHi ? *reinterpret_cast<const uint4 *>(hp2 + off)
+                             : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                mma_bf16(acc[(2 * w) % kAcc], hv[w].x, hv2[w].x, hv[w].y, hv2[w].y, buf[b][w].x,
+                         buf[b][w].y);
+                mma_bf16(acc[(2 * w + 1) % kAcc], hv[w].z, hv2[w].z, hv[w].w, hv2[w].w,
+                         buf[b][w].z, buf[b][w].w);
             }
             const int cn = c + NB;
             if (cn < CC) {
@@ -209,11 +219,13 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_mma_kernel(const ArgmaxArg
                 load_chunk(buf[b], gp + (size_t)kTile * KC, cn - CC);
             }
         }
-        float d0 = acc[0][0], d1 = acc[0][1];
+        float d0 = acc[0][0], d1 = acc[0][1], d2 = acc[0][2], d3 = acc[0][3];
 #pragma unroll
         for (int i = 1; i < kAcc; ++i) {
             d0 += acc[i][0];
             d1 += acc[i][1];
+            d2 += acc[i][2];
+            d3 += acc[i][3];
         }
 #pragma unroll
         for (int i = 0; i < kAcc; ++i)
@@ -224,6 +236,12 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_mma_kernel(const ArgmaxArg
             if (ra + 1 < nrows)
                 best.insert(make_key(d1, idb));
         }
+        if (hrow2) {
+            if (ra < nrows)
+                best2.insert(make_key(d2, ida));
+            if (ra + 1 < nrows)
+                best2.insert(make_key(d3, idb));
+        }
         gp += (size_t)kTile * KC;
         vcur = vnext;
     }
@@ -232,6 +250,11 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_mma_kernel(const ArgmaxArg
 #pragma unroll
         for (int i = 0; i < KM; ++i)
             s_cand[(g * kLists + warp * 4 + q) * KM + i] = best.v[i];
+    }
+    if (hrow2) {
+#pragma unroll
+        for (int i = 0; i < KM; ++i)
+            s_cand[((g + 8) * kLists + warp * 4 + q) * KM + i] = best2.v[i];
     }
     __syncthreads();
     block_finish<KM>(s_cand, M, kLists, a);

@@ -167,9 +167,9 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
         const cudaError_t e = device_info(&di);
         if (e != cudaSuccess)
             return cuda_failed(e);
-        if (bf16_uses_mma(hd->w, hd->N, hd->K, M, di.sms)) {
-            // 3..8 rows on a long head: one pass on the register-path tensor
-            // cores
+        if (bf16_uses_mma(hd->w, hd->N, hd->K, M, kmax, di.sms)) {
+            // 3..16 rows on a long head: one pass on the register-path
+            // tensor cores
             a.h = static_cast<const uint16_t *>(h);
             a.ids = ids;
             a.logits = logits;
@@ -354,7 +354,7 @@ dvl_status dvl_draft_plan(const dvl_head *head, int32_t M, int32_t k, const char
         const cudaError_t e = device_info(&di);
         if (e != cudaSuccess)
             return cuda_failed(e);
-        if (bf16_uses_mma(head->w, head->N, head->K, M, di.sms)) {
+        if (bf16_uses_mma(head->w, head->N, head->K, M, k == 1 ? 1 : DVL_MAX_TOPK, di.sms)) {
             *kernel = "bf16-mma";
             *launches = 1;
             return DVL_OK;

@@ -56,12 +56,13 @@ cudaError_t launch_argmax_bf16(const ArgmaxArgs &a, int M, int kmax, cudaStream_
 cudaError_t launch_argmax_lowbit(const ArgmaxArgs &a, int dtype, int M, int kmax,
                                  cudaStream_t s);
 int max_chunk_rows_bf16(int K);
-// Whether a call with M hidden rows runs on the register-path tensor cores
+// Whether a call with M hidden rows (kmax 1: argmax, 4: top-k) runs on the
+// register-path tensor cores
 // (argmax_bf16_mma.cuh) rather than the CUDA cores (M <= 4) or the tcgen05
 // kernel (M >= 5), for a head at w with N rows of width K on a device with
 // sms SMs.
-bool bf16_uses_mma(const void *w, int N, int K, int M, int sms);
-// That kernel, for M = 3 .. 8 hidden rows (K 2,560 or 5,120).
+bool bf16_uses_mma(const void *w, int N, int K, int M, int kmax, int sms);
+// That kernel, for M = 3 .. 16 hidden rows (3 .. 8 at K 5,120 and for top-k).
 cudaError_t launch_argmax_bf16_mma(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
 // Tensor-core argmax / top-k (bf16; kmax 1 or 4) for 5..32 hidden rows in
 // one launch.

@@ -188,9 +188,10 @@ dvl_status dvl_draft_topk(const dvl_head *head, const void *h, int32_t M, int32_
  * a static string owned by the library:
  *   "bf16-cuda-cores"  CUDA-core kernel (one or two hidden rows, widths
  *                      other than 2,560 / 5,120, short heads);
- *   "bf16-mma"         register-path tensor cores (3 .. 8 hidden rows,
- *                      width 2,560 or 5,120, a 32-byte aligned head of at
- *                      least 8 rows per warp of the grid);
+ *   "bf16-mma"         register-path tensor cores (3 .. 8 hidden rows at
+ *                      width 2,560 or 5,120, and argmax at 9 .. 16 rows at
+ *                      2,560, on a 32-byte aligned head of at least 8 rows
+ *                      per warp of the grid);
  *   "bf16-tcgen05"     5th-generation tensor cores (5 .. 32 hidden rows, when
  *                      the register-path kernel does not apply);
  *   "nvfp4-mma", "fp8-mma"  the low-bit heads.

@@ -1,7 +1,7 @@
-"""GPU parity of the register-path tensor-core kernel for bf16 heads (three
-to eight hidden rows, widths 2,560 and 5,120, heads of at least one full
-8-row tile per warp), against the oracle: bit-exact argmax and top-4 on
-integer heads with a d2t map and with id_base, ragged tiles at the end of
+"""GPU parity of the register-path tensor-core kernel for bf16 heads (3 .. 16
+hidden rows at width 2,560, 3 .. 8 at 5,120, heads of at least one full
+8-row tile per warp; top-k above 8 rows runs on the tcgen05 kernel),
+against the oracle: bit-exact argmax and top-4 on integer heads with a d2t map and with id_base, ragged tiles at the end of
 each warp's range, the same head one row short of the threshold (CUDA
 cores), a head that is 16-byte but not 32-byte aligned (CUDA cores),
 gaussian heads under the parity rule, and the plan each case reports."""
@@ -47,8 +47,8 @@ def int_case(seed, N, K, M):
     return rng, w, h
 
 
-@pytest.mark.parametrize("K", [2560, 5120])
-@pytest.mark.parametrize("M", [3, 4, 5, 8])
+@pytest.mark.parametrize("K,M", [(2560, 3), (2560, 4), (2560, 5), (2560, 8), (2560, 12), (2560, 16),
+                                 (5120, 3), (5120, 4), (5120, 5), (5120, 8)])
 def test_mma_integer_head_bit_exact(dvl, oracle_mod, K, M):
     N = threshold_rows() + 555  # ragged: warps end on partial tiles
     rng, w, h = int_case(K + M, N, K, M)
@@ -110,8 +110,14 @@ def test_mma_and_cuda_core_paths_agree_and_dispatch(dvl, oracle_mod):
     assert dvl.draft_plan(head, 2, 4) == ("bf16-cuda-cores", 1)
     assert dvl.draft_plan(head, 4) == ("bf16-mma", 1)
     assert dvl.draft_plan(head, 8, 4) == ("bf16-mma", 1)
-    assert dvl.draft_plan(head, 9) == ("bf16-tcgen05", 1)
+    assert dvl.draft_plan(head, 9) == ("bf16-mma", 1)
+    assert dvl.draft_plan(head, 16) == ("bf16-mma", 1)
+    assert dvl.draft_plan(head, 9, 4) == ("bf16-tcgen05", 1)
+    assert dvl.draft_plan(head, 17) == ("bf16-tcgen05", 1)
     assert dvl.draft_plan(head, 32, 4) == ("bf16-tcgen05", 1)
+    wide = dvl.Head(torch.empty((T, 5120), dtype=torch.int16, device="cuda"))
+    assert dvl.draft_plan(wide, 8) == ("bf16-mma", 1)
+    assert dvl.draft_plan(wide, 9) == ("bf16-tcgen05", 1)
     short = dvl.Head(cases["short"][0])
     assert dvl.draft_plan(short, 8) == ("bf16-tcgen05", 1)
     torch.cuda.synchronize()
@@ -119,7 +125,8 @@ def test_mma_and_cuda_core_paths_agree_and_dispatch(dvl, oracle_mod):
 
 
 @pytest.mark.parametrize("N,K,M", [(20011, 2560, 3), (32768, 5120, 4), (40000, 2560, 4),
-                                   (52755, 2560, 8), (20011, 5120, 6)])
+                                   (52755, 2560, 8), (20011, 5120, 6), (52755, 2560, 16),
+                                   (24000, 2560, 11)])
 def test_mma_gaussian_head_parity(dvl, oracle_mod, N, K, M):
     if N < threshold_rows():
         pytest.skip("head below the tensor-core threshold on this device")
