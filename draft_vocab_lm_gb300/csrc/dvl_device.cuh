@@ -250,13 +250,23 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
                                               row + (size_t)c * KM) + i)
                                         : make_ulonglong2(0ull, 0ull);
                 }
+                // each block's list is sorted best first: once one of its
+                // keys loses to the current k-th best, so does the rest
 #pragma unroll
-                for (int u = 0; u < kBatch; ++u)
+                for (int u = 0; u < kBatch; ++u) {
+                    uint64_t key[KM];
 #pragma unroll
                     for (int i = 0; i < KM / 2; ++i) {
-                        L.insert(v[u][i].x);
-                        L.insert(v[u][i].y);
+                        key[2 * i] = v[u][i].x;
+                        key[2 * i + 1] = v[u][i].y;
                     }
+#pragma unroll
+                    for (int i = 0; i < KM; ++i) {
+                        if (key[i] <= L.v[KM - 1])
+                            break;
+                        L.insert(key[i]);
+                    }
+                }
             }
         };
         auto write_row = [&](const TopList<KM> &F, int m) {
