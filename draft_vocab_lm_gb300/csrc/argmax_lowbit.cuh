@@ -56,12 +56,12 @@ constexpr int kChunk = 128;    // weights per row per k chunk
 constexpr int kFmtNvfp4 = 0, kFmtFp8 = 1;
 // 16-byte code loads per row per chunk per lane, code bytes per row per
 // k chunk, and k chunks of loads in flight per lane: 4 (measured against 2
-// and 5; ~4.5 KB per warp for NVFP4, ~8 KB for FP8), except 2 for FP8
-// top-k, whose lists leave no room for a deeper ring
+// and 5; ~4.5 KB per warp for NVFP4, ~8 KB for FP8).  Top-k keeps its
+// lists in shared memory, so it affords the same ring as argmax.
 template <int FMT> __host__ __device__ constexpr int q_words() { return FMT == kFmtFp8 ? 2 : 1; }
 template <int FMT> __host__ __device__ constexpr int chunk_bytes() { return FMT == kFmtFp8 ? 128 : 64; }
 template <int FMT, int KC, int KM>
-__host__ __device__ constexpr int ring_depth() { return FMT == kFmtFp8 && KM > 1 ? 2 : 4; }
+__host__ __device__ constexpr int ring_depth() { return 4; }
 constexpr int kLists = kWarps * 8;  // candidate lists per hidden row (8 row pairs per warp)
 
 // Four bytes of codes -> four f16x2 (byte t: low nibble in the low half).
@@ -309,9 +309,27 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
         prologue();
     const float down = (shift >= 0 ? pow2f(max(-shift, -126)) : pow2f(min(-shift, 127))) * a.gscale;
 
-    TopList<KM> best0, best1;  // hidden rows 2q and 2q + 1
+    // argmax: the best key of hidden rows 2q and 2q + 1 in registers; top-k:
+    // the lists in this lane's own candidate slots in shared memory (zeroed
+    // above), which the block merge reads at the end
+    TopList<1> best0, best1;
     best0.init();
     best1.init();
+    const int slot = warp * 8 + g;
+    uint64_t *list0 = s_cand + ((size_t)(2 * q) * kLists + slot) * KM;
+    uint64_t *list1 = s_cand + ((size_t)(2 * q + 1) * kLists + slot) * KM;
+    auto keep0 = [&](uint64_t key) {
+        if constexpr (KM == 1)
+            best0.insert(key);
+        else
+            list_insert_smem<KM>(list0, key);
+    };
+    auto keep1 = [&](uint64_t key) {
+        if constexpr (KM == 1)
+            best1.insert(key);
+        else
+            list_insert_smem<KM>(list1, key);
+    };
     // four independent accumulators, so consecutive MMAs do not wait on
     // each other; summed at the end of a group
     float acc[4][4];
@@ -389,15 +407,15 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
         }
         if (ra < rend) {
             if (2 * q < M)
-                best0.insert(make_key(d[0] * down, ida));
+                keep0(make_key(d[0] * down, ida));
             if (2 * q + 1 < M)
-                best1.insert(make_key(d[1] * down, ida));
+                keep1(make_key(d[1] * down, ida));
         }
         if (rb < rend) {
             if (2 * q < M)
-                best0.insert(make_key(d[2] * down, idb));
+                keep0(make_key(d[2] * down, idb));
             if (2 * q + 1 < M)
-                best1.insert(make_key(d[3] * down, idb));
+                keep1(make_key(d[3] * down, idb));
         }
     };
     auto row_id = [&](int r) {
@@ -492,16 +510,11 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
         }
     }
 
-    const int slot = warp * 8 + g;
-    if (2 * q < M) {
-#pragma unroll
-        for (int i = 0; i < KM; ++i)
-            s_cand[((2 * q) * kLists + slot) * KM + i] = best0.v[i];
-    }
-    if (2 * q + 1 < M) {
-#pragma unroll
-        for (int i = 0; i < KM; ++i)
-            s_cand[((2 * q + 1) * kLists + slot) * KM + i] = best1.v[i];
+    if constexpr (KM == 1) {
+        if (2 * q < M)
+            list0[0] = best0.v[0];
+        if (2 * q + 1 < M)
+            list1[0] = best1.v[0];
     }
     __syncthreads();
     block_finish<KM>(s_cand, M, kLists, a);

@@ -93,6 +93,24 @@ struct TopList {
     }
 };
 
+// Insert key into a sorted (best first) list of KM keys in shared memory
+// that only the calling thread uses; most keys lose to the last entry and
+// cost one read.
+template <int KM>
+__device__ __forceinline__ void list_insert_smem(uint64_t *lst, uint64_t key)
+{
+    if (key <= lst[KM - 1])
+        return;
+    TopList<KM> t;
+#pragma unroll
+    for (int i = 0; i < KM; ++i)
+        t.v[i] = lst[i];
+    t.insert(key);
+#pragma unroll
+    for (int i = 0; i < KM; ++i)
+        lst[i] = t.v[i];
+}
+
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t x)
 {
 #pragma unroll
