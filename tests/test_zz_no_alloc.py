@@ -49,7 +49,9 @@ def test_noalloc_argmax_matches_the_workspace_entry_point_twice(dvl):
     st = head.struct()
     stream = torch.cuda.current_stream().cuda_stream
 
-    for call, M in enumerate((3, 5)):
+    # 3, 5 and 16 rows run on the register-path tensor cores (20,000 rows is
+    # a long enough head on a 152-SM GB300), 32 on tcgen05
+    for call, M in enumerate((3, 5, 16, 32)):
         h = dev(S.hidden_bf16(100 + call, M, K))
         ids = torch.full((M,), -9, dtype=torch.int32, device="cuda")
         vals = torch.zeros(M, dtype=torch.float32, device="cuda")
