@@ -144,3 +144,28 @@ def test_fp8_fullvocab_argmax_and_top4(dvl, oracle_mod, fp8_full, M):
     print(f"[parity] fp8 full vocab M={M}: {rep}")
     ids, vals = dvl.draft_topk(head, dev(h), 4, ws=dvl.make_workspace(M, 4))
     check_topk(oracle_mod, L, None, 4, ids.cpu().numpy(), vals.cpu().numpy())
+
+
+@pytest.mark.parametrize("K,M", [(2560, 1), (5120, 3)])
+def test_fp8_head_16_byte_aligned_only(dvl, oracle_mod, K, M):
+    # the same rows at a 32-byte aligned address and 16 bytes into a buffer
+    # (the least alignment a head may have): identical, exact results
+    N = 3001
+    rng = np.random.default_rng(K + M + 5)
+    q, _ = _int_e4m3(rng, (N, K))
+    h = S.f32_to_bf16_bits(rng.integers(-8, 9, size=(M, K)).astype(np.float32))
+    flat = torch.empty(N * K + 16, dtype=torch.uint8, device="cuda")
+    flat[16:] = dev(q).view(-1)
+    q16 = flat[16:].view(N, K)
+    assert q16.data_ptr() % 32 == 16
+    L, _ = oracle_mod.logits_fp8(q, 0.5, h)
+    for wq in (dev(q), q16):
+        head = dvl.Head(wq, fmt="fp8", global_scale=0.5)
+        ids, vals = dvl.draft_topk(head, dev(h), 4)
+        o_ids, o_vals, _ = oracle_mod.topk(L, 4, None)
+        assert np.array_equal(ids.cpu().numpy(), o_ids)
+        assert np.array_equal(vals.cpu().numpy(), o_vals)
+        ids, vals = dvl.draft_argmax(head, dev(h))
+        o_ids, o_vals = oracle_mod.argmax(L, None)
+        assert np.array_equal(ids.cpu().numpy(), o_ids)
+        assert np.array_equal(vals.cpu().numpy(), o_vals)
