@@ -70,6 +70,16 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// 32-byte load of weights read exactly once (no L1 allocation, 256-byte L2
+// fetch); lo holds the lower 16 bytes.
+__device__ __forceinline__ void ld_stream32(const void *p, uint4 &lo, uint4 &hi)
+{
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z),
+          "=r"(hi.w)
+        : "l"(p));
+}
+
 __device__ __forceinline__ void cp_async16(void *dst, const void *src)
 {
     const unsigned d = (unsigned)__cvta_generic_to_shared(dst);

@@ -21,18 +21,6 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p)
     return v;
 }
 
-// 32-byte load of weights read exactly once (no L1 allocation, 256-byte L2
-// fetch); lo holds the lower 16 bytes.  The address must be 32-byte aligned.
-// Four lanes reading consecutive 32 bytes fill one 128-byte line per
-// instruction, where 16-byte loads fill half of each of two lines.
-__device__ __forceinline__ void ld_stream32(const void *p, uint4 &lo, uint4 &hi)
-{
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-        : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z),
-          "=r"(hi.w)
-        : "l"(p));
-}
-
 // Programmatic dependent launch: allow the next kernel on the stream to
 // start launching; wait until the preceding kernel has completed and its
 // memory operations are visible.  Both are no-ops without a dependency.
