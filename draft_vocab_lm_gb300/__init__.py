@@ -48,6 +48,23 @@ def _stream_handle(stream, device) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+_raw_stream_fn = None
+
+
+def _call_stream(stream, t) -> int:
+    """The stream handle for a draft call on tensor t's device: the given
+    stream, or the device's current one.  A short draft call takes about as
+    long on the GPU as building a torch Stream object takes on the host, so
+    the current stream is read as a raw handle when torch offers that."""
+    global _raw_stream_fn
+    if stream is None:
+        if _raw_stream_fn is None:
+            _raw_stream_fn = getattr(_torch()._C, "_cuda_getCurrentRawStream", False)
+        if _raw_stream_fn:
+            return int(_raw_stream_fn(t.get_device()))
+    return _stream_handle(stream, t.device)
+
+
 def version() -> int:
     return int(lib().dvl_version())
 
@@ -193,37 +210,35 @@ def _check_h(head: Head, h):
 
 def draft_topk(head: Head, h, k: int, *, ids=None, logits=None, ws=None, stream=None):
     """Per hidden row: the k best (full id, logit), best first."""
-    torch = _torch()
     _check_h(head, h)
     M = h.shape[0]
     if ids is None:
-        ids = torch.empty((M, k), dtype=torch.int32, device=h.device)
+        ids = _torch().empty((M, k), dtype=_torch().int32, device=h.device)
     if logits is None:
-        logits = torch.empty((M, k), dtype=torch.float32, device=h.device)
+        logits = _torch().empty((M, k), dtype=_torch().float32, device=h.device)
     if ws is None:
         ws = make_workspace(M, k, device=h.device, stream=stream)
     check("dvl_draft_topk",
           lib().dvl_draft_topk(ctypes.byref(head.struct()), h.data_ptr(), M, int(k), ids.data_ptr(),
                                logits.data_ptr(), ws.data_ptr(), ws.numel(),
-                               _stream_handle(stream, h.device)))
+                               _call_stream(stream, h)))
     return ids, logits
 
 
 def draft_argmax(head: Head, h, *, ids=None, logits=None, ws=None, stream=None):
     """Per hidden row: (full id, max logit) of the best head row."""
-    torch = _torch()
     _check_h(head, h)
     M = h.shape[0]
     if ids is None:
-        ids = torch.empty(M, dtype=torch.int32, device=h.device)
+        ids = _torch().empty(M, dtype=_torch().int32, device=h.device)
     if logits is None:
-        logits = torch.empty(M, dtype=torch.float32, device=h.device)
+        logits = _torch().empty(M, dtype=_torch().float32, device=h.device)
     if ws is None:
         ws = make_workspace(M, 1, device=h.device, stream=stream)
     check("dvl_draft_argmax",
           lib().dvl_draft_argmax(ctypes.byref(head.struct()), h.data_ptr(), M, ids.data_ptr(),
                                  logits.data_ptr(), ws.data_ptr(), ws.numel(),
-                                 _stream_handle(stream, h.device)))
+                                 _call_stream(stream, h)))
     return ids, logits
 
 
