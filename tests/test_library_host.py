@@ -252,3 +252,17 @@ def test_plan_without_a_device(dvl):
     nv = _head(dtype=DVL_NVFP4, scales=0x7000, K=5120)
     assert L.dvl_draft_plan(ctypes.byref(nv), 32, 4, ctypes.byref(name), ctypes.byref(n)) == 0
     assert name.value == b"nvfp4-mma" and n.value >= 4
+
+
+def test_call_stream_handle_without_a_device(dvl, monkeypatch):
+    # an explicit stream (object or raw handle) is passed through unchanged;
+    # the current stream is read as a raw handle when torch offers that
+    import types
+    import draft_vocab_lm_gb300 as d
+    torch = pytest.importorskip("torch")
+    t = torch.zeros(1)
+    assert d._call_stream(types.SimpleNamespace(cuda_stream=1234), t) == 1234
+    assert d._call_stream(77, t) == 77
+    monkeypatch.setattr(d, "_raw_stream_fn", lambda dev_index: 4242 + dev_index)
+    t.get_device = lambda: 0  # a CPU tensor reports -1
+    assert d._call_stream(None, t) == 4242
