@@ -97,10 +97,4 @@ __device__ __forceinline__ uint4 lds128(const void *p)
     return v;
 }
 
-// Record a device-side failure in the workspace status word.
-__device__ __forceinline__ void set_status(unsigned char *ws, unsigned int code)
-{
-    atomicOr(reinterpret_cast<unsigned int *>(ws + kWsStatus), code);
-}
-
 }  // namespace dvl

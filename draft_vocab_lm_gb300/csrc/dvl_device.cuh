@@ -67,6 +67,31 @@ __device__ __forceinline__ int32_t key_id(uint64_t key)
     return (int32_t)(0xffffffffu - (uint32_t)key);  // empty slot -> -1
 }
 
+// Record a device-side failure in the workspace status word.
+__device__ __forceinline__ void set_status(unsigned char *ws, unsigned int code)
+{
+    atomicOr(reinterpret_cast<unsigned int *>(ws + kWsStatus), code);
+}
+
+// Full-vocabulary id of head row `row`: d2t[row], or id_base + row without
+// a d2t.  Nothing is ever read through the id.
+__device__ __forceinline__ int32_t full_id(const ArgmaxArgs &a, int row)
+{
+    return a.d2t ? __ldg(a.d2t + row) : (int32_t)(a.id_base + row);
+}
+
+// Write result i (id and logit) of a call.  An id outside [0, V) -- a d2t
+// entry out of range -- is written as it is and reported as
+// DVL_ERR_OUT_OF_RANGE in the workspace status word.
+__device__ __forceinline__ void put_result(const ArgmaxArgs &a, int i, uint64_t key)
+{
+    const int32_t id = key_id(key);
+    if ((uint32_t)id >= (uint32_t)a.V)  // V <= 2^31 - 1; a negative id wraps high
+        set_status(a.ws, 1u << DVL_ERR_OUT_OF_RANGE);
+    a.ids[i] = id;
+    a.logits[i] = key_logit(key);
+}
+
 // A descending list of the KM best keys seen by one lane.
 template <int KM>
 struct TopList {
@@ -243,9 +268,7 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
     if constexpr (KM == 1) {
         // one thread per hidden row: the swaps go out together
         for (int m = threadIdx.x; m < M; m += blockDim.x) {
-            uint64_t key = atomicExch(best + m, 0ull);
-            a.ids[m] = key_id(key);
-            a.logits[m] = key_logit(key);
+            put_result(a, m, atomicExch(best + m, 0ull));
         }
     } else {
         // The slots are [M][blocks][KM]: one hidden row's lists are
@@ -293,8 +316,7 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
 #pragma unroll
                 for (int i = 1; i < KM; ++i)
                     key = lane == i ? F.v[i] : key;
-                a.ids[m * a.k + lane] = key_id(key);
-                a.logits[m * a.k + lane] = key_logit(key);
+                put_result(a, m * a.k + lane, key);
             }
         };
         if (M >= nwarps) {
@@ -314,8 +336,7 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
 #pragma unroll
                 for (int i = 1; i < KM; ++i)
                     key = sub == i ? L.v[i] : key;
-                a.ids[m * a.k + sub] = key_id(key);
-                a.logits[m * a.k + sub] = key_logit(key);
+                put_result(a, m * a.k + sub, key);
             }
         } else {
             // nwarps / M warps per hidden row, merged through shared memory

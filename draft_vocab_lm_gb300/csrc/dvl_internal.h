@@ -14,7 +14,7 @@ namespace dvl {
 // it: the ticket wraps back to 0 and the best keys are exchanged back to 0.
 constexpr int kMaxCtas = 1024;            // grid cap of every reducing kernel
 constexpr size_t kWsTicket = 0;           // uint32: blocks finished so far
-constexpr size_t kWsStatus = 4;           // uint32: reserved for device checks
+constexpr size_t kWsStatus = 4;           // uint32: device-side failure bits (1 << dvl_status)
 constexpr size_t kWsAmax = 8;             // uint32: a head's max |w| while it is requantized
 constexpr size_t kWsBest = 256;           // uint64[DVL_MAX_M]: best key per row (k = 1)
 constexpr size_t kWsSlots = 512;          // uint64[kMaxCtas][M][kmax] (k > 1)
@@ -33,6 +33,7 @@ struct ArgmaxArgs {
     int k;                    // results per row (1 .. kmax)
     unsigned char *ws;        // workspace base
     bool head_static;         // w / scales / d2t not written by pending work
+    int32_t V;                // vocabulary size (<= 2^31 - 1): ids lie in [0, V)
 };
 
 // Per-device facts, queried once.
