@@ -73,13 +73,6 @@ __device__ __forceinline__ void set_status(unsigned char *ws, unsigned int code)
     atomicOr(reinterpret_cast<unsigned int *>(ws + kWsStatus), code);
 }
 
-// Full-vocabulary id of head row `row`: d2t[row], or id_base + row without
-// a d2t.  Nothing is ever read through the id.
-__device__ __forceinline__ int32_t full_id(const ArgmaxArgs &a, int row)
-{
-    return a.d2t ? __ldg(a.d2t + row) : (int32_t)(a.id_base + row);
-}
-
 // Write result i (id and logit) of a call.  An id outside [0, V) -- a d2t
 // entry out of range -- is written as it is and reported as
 // DVL_ERR_OUT_OF_RANGE in the workspace status word.
