@@ -354,7 +354,11 @@ cudaError_t launch_m(const ArgmaxArgs &a, cudaStream_t s)
         else
             return launch_cfg<M, KM, 5120, 2, 4>(a, s);
     }
-    return launch_cfg<M, KM, 0, 2, 4>(a, s);
+    // (run-time K, four hidden rows, top-k: two rows per group; four spill)
+    if constexpr (M == 4 && KM > 1)
+        return launch_cfg<M, KM, 0, 2, 2>(a, s);
+    else
+        return launch_cfg<M, KM, 0, 2, 4>(a, s);
 }
 
 inline int kpad_of(int K) { return (K + kKStep - 1) / kKStep * kKStep; }

@@ -60,8 +60,13 @@ constexpr int kFmtNvfp4 = 0, kFmtFp8 = 1;
 // lists in shared memory, so it affords the same ring as argmax.
 template <int FMT> __host__ __device__ constexpr int q_words() { return FMT == kFmtFp8 ? 2 : 1; }
 template <int FMT> __host__ __device__ constexpr int chunk_bytes() { return FMT == kFmtFp8 ? 128 : 64; }
-template <int FMT, int KC, int KM>
-__host__ __device__ constexpr int ring_depth() { return 4; }
+template <int FMT, int M, int KC, int KM>
+__host__ __device__ constexpr int ring_depth()
+{
+    // FP8 argmax with four hidden rows at 5,120 spills registers with a
+    // 4-deep ring (ptxas); a 2-deep one keeps it within 128
+    return (FMT == kFmtFp8 && M >= 4 && KC == 5120 && KM == 1) ? 2 : 4;
+}
 constexpr int kLists = kWarps * 8;  // candidate lists per hidden row (8 row pairs per warp)
 
 // Four bytes of codes -> four f16x2 (byte t: low nibble in the low half).
@@ -130,7 +135,7 @@ __host__ __device__ inline size_t lowbit_h_bytes(int Kpad, int M) { return (size
 template <int FMT, int M, int KM, int KC>
 __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const ArgmaxArgs a)
 {
-    constexpr int kNB = ring_depth<FMT, KC, KM>(), kQW = q_words<FMT>();
+    constexpr int kNB = ring_depth<FMT, M, KC, KM>(), kQW = q_words<FMT>();
     constexpr bool kNv = FMT == kFmtNvfp4;
     extern __shared__ __align__(16) unsigned char smem[];
     const int K = KC > 0 ? KC : a.K;
