@@ -133,6 +133,7 @@ class Head:
         self.static = bool(static)
         self.device = w.device
         self._struct = None
+        self._on_enqueue = None  # called after a draft call with this head is enqueued
 
     def struct(self) -> DvlHead:
         if self._struct is None:
@@ -222,6 +223,8 @@ def draft_topk(head: Head, h, k: int, *, ids=None, logits=None, ws=None, stream=
           lib().dvl_draft_topk(ctypes.byref(head.struct()), h.data_ptr(), M, int(k), ids.data_ptr(),
                                logits.data_ptr(), ws.data_ptr(), ws.numel(),
                                _call_stream(stream, h)))
+    if head._on_enqueue is not None:
+        head._on_enqueue()
     return ids, logits
 
 
@@ -239,6 +242,8 @@ def draft_argmax(head: Head, h, *, ids=None, logits=None, ws=None, stream=None):
           lib().dvl_draft_argmax(ctypes.byref(head.struct()), h.data_ptr(), M, ids.data_ptr(),
                                  logits.data_ptr(), ws.data_ptr(), ws.numel(),
                                  _call_stream(stream, h)))
+    if head._on_enqueue is not None:
+        head._on_enqueue()
     return ids, logits
 
 
@@ -345,8 +350,9 @@ class Shortlist:
     ("Masked MTP drafts", section "Update (November 2026)": a static trim can
     miss; learning the escaped ids into spare head rows recovered the loss.)
     The head is trimmed to `ranks` into buffers of `capacity` rows; learn()
-    appends the full head's rows of ids the list does not hold yet, in stream
-    order, until the spare rows run out.
+    hands the emitted ids to dvl_learn_missing, which appends the full
+    head's rows of the ids the list does not hold yet, in stream order,
+    until the spare rows run out.
 
         sl = Shortlist(w_full, ranks, capacity=len(ranks) + 1024)
         ids, logits = draft_argmax(sl.head(), h)
@@ -371,18 +377,15 @@ class Shortlist:
             self.scales = torch.empty((capacity, scales.shape[1]), dtype=scales.dtype,
                                       device=scales.device)
         self.d2t = torch.empty(capacity, dtype=torch.int32, device=w_full.device)
-        self.row_of = np.full(self.V, -1, dtype=np.int64)  # full id -> trimmed row
-        self.n = 0
-        self._pending = False
-        self._append(r)
-
-    def _append(self, ids: np.ndarray) -> None:
-        learn_rows(self.w_full, ids, self.w, self.d2t, self.n, scales=self.scales_full,
+        # full id -> trimmed row (-1: not in the list), the table the C call keeps
+        self.row_of = np.full(self.V, -1, dtype=np.int32)
+        learn_rows(self.w_full, r, self.w, self.d2t, 0, scales=self.scales_full,
                    scales_trim=self.scales, fmt=self.fmt, stream=self.stream)
-        fresh = self.row_of[ids] < 0
-        self.row_of[ids[fresh]] = self.n + np.nonzero(fresh)[0]
-        self.n += ids.shape[0]
-        self._pending = True
+        # a padded list may repeat ids: each maps to its first row
+        first = np.unique(r, return_index=True)
+        self.row_of[first[0]] = first[1].astype(np.int32)
+        self.n = int(r.shape[0])
+        self._pending = True  # rows written by kernels that may still run
 
     def learn(self, ids) -> np.ndarray:
         """Learn the ids (host, any order, repeats allowed) the list does not
@@ -390,22 +393,42 @@ class Shortlist:
         x = np.asarray(ids, dtype=np.int64).ravel()
         if x.size and (x.min() < 0 or x.max() >= self.V):
             raise ValueError("ids outside the vocabulary")
-        x = x[self.row_of[x] < 0]
-        x = x[np.sort(np.unique(x, return_index=True)[1])]  # first occurrences, in order
-        x = x[:self.capacity - self.n].astype(np.int32)
-        if x.size:
-            self._append(x)
-        return x
+        x = np.ascontiguousarray(x.astype(np.int32))
+        learned = np.empty(max(1, x.size), dtype=np.int32)
+        n_rows = ctypes.c_int32(self.n)
+        n_learned = ctypes.c_int32(0)
+        full = Head(self.w_full, scales=self.scales_full, fmt=self.fmt)
+        check("dvl_learn_missing",
+              lib().dvl_learn_missing(ctypes.byref(full.struct()),
+                                      x.ctypes.data if x.size else None, x.size,
+                                      self.row_of.ctypes.data, ctypes.byref(n_rows),
+                                      self.capacity, self.w.data_ptr(),
+                                      self.scales.data_ptr() if self.scales is not None else None,
+                                      self.d2t.data_ptr(), learned.ctypes.data,
+                                      ctypes.byref(n_learned),
+                                      _stream_handle(self.stream, self.w_full.device)))
+        self.n = int(n_rows.value)
+        if n_learned.value:
+            self._pending = True
+        return learned[:n_learned.value].copy()
+
+    def _enqueued(self) -> None:
+        # a draft call that waits for the stream's preceding work has been
+        # enqueued after the last learn: later calls may stream the head
+        # before their wait
+        self._pending = False
 
     def head(self, *, static: bool = True) -> Head:
-        """The active rows as a Head.  The first head handed out after a
-        learn is not static (the rows were written by the stream's latest
-        kernels); later ones are, unless static=False."""
+        """The active rows as a Head.  Heads handed out between a learn and
+        the first draft call enqueued after it are not static (the rows were
+        written by the stream's latest kernels); later ones are, unless
+        static=False."""
         hd = Head(self.w[:self.n], V=self.V, d2t=self.d2t[:self.n],
                   scales=self.scales[:self.n] if self.scales is not None else None,
                   global_scale=self.global_scale, static=static and not self._pending,
                   fmt=self.fmt)
-        self._pending = False
+        if self._pending:
+            hd._on_enqueue = self._enqueued
         return hd
 
 

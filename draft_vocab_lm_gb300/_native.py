@@ -30,9 +30,10 @@ STATUS_NAMES = {
 EXPORTS = (
     "dvl_status_string", "dvl_version", "dvl_last_error", "dvl_workspace_bytes", "dvl_workspace_init",
     "dvl_workspace_status",
-    "dvl_draft_argmax", "dvl_draft_topk", "dvl_draft_argmax_noalloc", "dvl_draft_plan",
+    "dvl_draft_argmax", "dvl_draft_topk", "dvl_draft_argmax_noalloc", "dvl_noalloc_status",
+    "dvl_draft_plan",
     "dvl_score_ids",
-    "dvl_trim_head", "dvl_learn_rows", "dvl_quantize_head",
+    "dvl_trim_head", "dvl_learn_rows", "dvl_learn_missing", "dvl_quantize_head",
     "dvl_histogram",
     "dvl_build_ranks", "dvl_union_sorted",
 )
@@ -91,17 +92,21 @@ def lib():
         L.dvl_workspace_status.argtypes = [p, p, p]
         L.dvl_draft_argmax.argtypes = [hp, p, i32, p, p, p, sz, p]
         L.dvl_draft_topk.argtypes = [hp, p, i32, i32, p, p, p, sz, p]
+        L.dvl_draft_argmax_noalloc.argtypes = [hp, p, i32, p, p, p]
+        L.dvl_noalloc_status.argtypes = [p, p]
         L.dvl_draft_plan.argtypes = [hp, i32, i32, p, p]
         L.dvl_score_ids.argtypes = [hp, p, i32, p, i32, p, p]
         L.dvl_trim_head.argtypes = [hp, p, i32, p, p, p, p, p]
         L.dvl_learn_rows.argtypes = [hp, p, i32, i32, p, p, p, p]
+        L.dvl_learn_missing.argtypes = [hp, p, i32, p, p, i32, p, p, p, p, p, p]
         L.dvl_quantize_head.argtypes = [hp, i32, p, p, p, p, sz, p]
         L.dvl_histogram.argtypes = [p, i64, i64, p]
         L.dvl_build_ranks.argtypes = [p, i64, p, i32, i32, i32, p, p]
         L.dvl_union_sorted.argtypes = [p, i32, p, i32, p, p]
         for fn in ("dvl_workspace_init", "dvl_workspace_status", "dvl_draft_argmax", "dvl_draft_topk",
+                   "dvl_draft_argmax_noalloc", "dvl_noalloc_status",
                    "dvl_draft_plan", "dvl_score_ids",
-                   "dvl_trim_head", "dvl_learn_rows", "dvl_quantize_head", "dvl_histogram", "dvl_build_ranks", "dvl_union_sorted"):
+                   "dvl_trim_head", "dvl_learn_rows", "dvl_learn_missing", "dvl_quantize_head", "dvl_histogram", "dvl_build_ranks", "dvl_union_sorted"):
             getattr(L, fn).restype = ctypes.c_int
         _lib = L
         return L

@@ -155,6 +155,7 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
     a.gscale = hd->global_scale;
     a.d2t = hd->d2t;
     a.id_base = hd->id_base;
+    a.V = (int32_t)hd->V;
     a.head_static = (hd->flags & DVL_HEAD_STATIC) != 0;
     a.N = hd->N;
     a.K = hd->K;
@@ -214,35 +215,29 @@ dvl_status check_reduce_args(const dvl_head *hd, const void *h, int32_t M, int32
     return DVL_OK;
 }
 
-// Rows row0 .. row0 + n - 1 of a trimmed head from the full head's rows
-// ids[0 .. n - 1] (host ids, checked first), and d2t[row0 + i] = ids[i].
-static dvl_status gather_rows(const dvl_head *full, const int32_t *ids, int32_t n,
-                              int32_t row0, void *w_trim, uint8_t *scales_trim, int32_t *d2t,
-                              int32_t *n_duplicates, void *stream)
+// The argument checks of a gather into a trimmed head's buffers.
+static dvl_status check_gather(const dvl_head *full, void *w_trim, uint8_t *scales_trim,
+                               int32_t *d2t)
 {
     dvl_status st = check_head(full);
     if (st != DVL_OK)
         return st;
     if ((int64_t)full->N != full->V || full->d2t || full->id_base != 0)
         return DVL_ERR_INVALID_ARG;
-    if (!ids || n < 1 || row0 < 0 || (int64_t)row0 + n > 0x7fffffffLL)
-        return DVL_ERR_INVALID_ARG;
     if (!w_trim || !aligned(w_trim, 16) || !d2t || !aligned(d2t, 4))
         return DVL_ERR_INVALID_ARG;
     if (full->dtype == DVL_NVFP4 && (!scales_trim || !aligned(scales_trim, 16)))
         return DVL_ERR_INVALID_ARG;
-    std::vector<unsigned char> seen((size_t)full->V, 0);
-    int32_t dup = 0;
-    for (int32_t i = 0; i < n; ++i) {
-        const int32_t r = ids[i];
-        if (r < 0 || (int64_t)r >= full->V)
-            return DVL_ERR_OUT_OF_RANGE;
-        if (seen[(size_t)r])
-            ++dup;
-        seen[(size_t)r] = 1;
-    }
-    if (n_duplicates)
-        *n_duplicates = dup;
+    return DVL_OK;
+}
+
+// Enqueue rows row0 .. row0 + n - 1 of a trimmed head from the full head's
+// rows ids[0 .. n - 1] (host ids, already checked), and d2t[row0 + i] =
+// ids[i].
+static dvl_status enqueue_gather(const dvl_head *full, const int32_t *ids, int32_t n,
+                                 int32_t row0, void *w_trim, uint8_t *scales_trim, int32_t *d2t,
+                                 void *stream)
+{
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int32_t *d2t_rows = d2t + row0;
     cudaError_t e =
@@ -258,6 +253,34 @@ static dvl_status gather_rows(const dvl_head *full, const int32_t *ids, int32_t 
         e = launch_trim_rows(full->scales, K / 16, scales_trim + (int64_t)row0 * (K / 16),
                              d2t_rows, n, s);
     return e == cudaSuccess ? DVL_OK : cuda_failed(e);
+}
+
+// Rows row0 .. row0 + n - 1 of a trimmed head from the full head's rows
+// ids[0 .. n - 1] (host ids, checked first), and d2t[row0 + i] = ids[i].
+// Repeated ids are counted only when n_duplicates asks for it (a V-byte
+// host table, which the load-time trim can afford and a learn need not).
+static dvl_status gather_rows(const dvl_head *full, const int32_t *ids, int32_t n,
+                              int32_t row0, void *w_trim, uint8_t *scales_trim, int32_t *d2t,
+                              int32_t *n_duplicates, void *stream)
+{
+    dvl_status st = check_gather(full, w_trim, scales_trim, d2t);
+    if (st != DVL_OK)
+        return st;
+    if (!ids || n < 1 || row0 < 0 || (int64_t)row0 + n > 0x7fffffffLL)
+        return DVL_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i)
+        if (ids[i] < 0 || (int64_t)ids[i] >= full->V)
+            return DVL_ERR_OUT_OF_RANGE;
+    if (n_duplicates) {
+        std::vector<unsigned char> seen((size_t)full->V, 0);
+        int32_t dup = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            dup += seen[(size_t)ids[i]];
+            seen[(size_t)ids[i]] = 1;
+        }
+        *n_duplicates = dup;
+    }
+    return enqueue_gather(full, ids, n, row0, w_trim, scales_trim, d2t, stream);
 }
 
 }  // namespace dvl
@@ -438,6 +461,45 @@ dvl_status dvl_learn_rows(const dvl_head *full, const int32_t *ids, int32_t n, i
                           void *w_trim, uint8_t *scales_trim, int32_t *d2t, void *stream)
 {
     return gather_rows(full, ids, n, row0, w_trim, scales_trim, d2t, nullptr, stream);
+}
+
+dvl_status dvl_learn_missing(const dvl_head *full, const int32_t *ids, int32_t n,
+                             int32_t *row_of, int32_t *n_rows, int32_t capacity, void *w_trim,
+                             uint8_t *scales_trim, int32_t *d2t, int32_t *learned,
+                             int32_t *n_learned, void *stream)
+{
+    dvl_status st = check_gather(full, w_trim, scales_trim, d2t);
+    if (st != DVL_OK)
+        return st;
+    if (n < 0 || (n > 0 && !ids) || !row_of || !n_rows || !learned || !n_learned)
+        return DVL_ERR_INVALID_ARG;
+    const int32_t row0 = *n_rows;
+    if (row0 < 0 || capacity < row0)
+        return DVL_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i)
+        if (ids[i] < 0 || (int64_t)ids[i] >= full->V)
+            return DVL_ERR_OUT_OF_RANGE;  // nothing changed, nothing enqueued
+    // first occurrences of ids the list lacks, in order, while rows remain
+    int32_t m = 0;
+    for (int32_t i = 0; i < n && row0 + m < capacity; ++i) {
+        const int32_t t = ids[i];
+        if (row_of[t] >= 0)
+            continue;
+        row_of[t] = row0 + m;  // also skips later repeats of t
+        learned[m++] = t;
+    }
+    *n_learned = m;
+    if (m == 0)
+        return DVL_OK;
+    st = enqueue_gather(full, learned, m, row0, w_trim, scales_trim, d2t, stream);
+    if (st != DVL_OK) {
+        for (int32_t i = 0; i < m; ++i)
+            row_of[learned[i]] = -1;  // undo: the rows were not written
+        *n_learned = 0;
+        return st;
+    }
+    *n_rows = row0 + m;
+    return DVL_OK;
 }
 
 const char *dvl_last_error(void) { return cudaGetErrorString(t_last_error); }

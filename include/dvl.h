@@ -53,11 +53,12 @@ extern "C" {
 typedef enum {
     DVL_OK = 0,
     DVL_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, misalignment        */
-    DVL_ERR_OUT_OF_RANGE = 2, /* an id outside [0, V)                        */
+    DVL_ERR_OUT_OF_RANGE = 2, /* an id outside [0, V) (host-checked ids; as a
+                                 device-side bit: a d2t entry outside [0, V)) */
     DVL_ERR_UNSUPPORTED = 3,  /* a shape this build has no kernel for        */
     DVL_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required  */
     DVL_ERR_CUDA = 5,         /* a CUDA runtime call or a launch failed      */
-    DVL_ERR_TIMEOUT = 6       /* reserved: a bounded device wait gave up     */
+    DVL_ERR_TIMEOUT = 6       /* device-side bit: a bounded wait gave up     */
 } dvl_status;
 
 typedef enum {
@@ -99,8 +100,12 @@ typedef struct dvl_head {
     float global_scale;   /* NVFP4 / FP8 tensor scale; ignored for bf16        */
     int32_t reserved2;    /* must be 0                                         */
     const int32_t *d2t;   /* int32 [N]: full-vocabulary id of each row, each in
-                             [0, V) (the kernels do not check); NULL means the
-                             identity map shifted by id_base                   */
+                             [0, V); NULL means the identity map shifted by
+                             id_base.  The kernels read no memory through a
+                             d2t entry; a returned id outside [0, V) is
+                             returned as it is and reported as the
+                             device-side status bit DVL_ERR_OUT_OF_RANGE (see
+                             dvl_workspace_status)                           */
 } dvl_head;
 
 /* Human-readable name of a status code (static storage). */
@@ -131,11 +136,13 @@ size_t dvl_workspace_bytes(int32_t M, int32_t k);
 dvl_status dvl_workspace_init(void *ws, size_t bytes, void *stream);
 
 /* Device-side failures recorded in a workspace since it was last read: a
- * bitmask with bit (1 << s) set for each dvl_status s a kernel reported.
- * Today the only one is DVL_ERR_TIMEOUT: a bounded wait of the tensor-core
- * argmax gave up, and that call's results are not valid.  The status word
- * is read after the work already enqueued on `stream` (this synchronizes
- * `stream`), then cleared on `stream`.
+ * bitmask with bit (1 << s) set for each dvl_status s a kernel reported:
+ *   DVL_ERR_TIMEOUT       a bounded wait of the tcgen05 kernel gave up; that
+ *                         call's results are not valid;
+ *   DVL_ERR_OUT_OF_RANGE  a draft call returned an id outside [0, V): a d2t
+ *                         entry out of range won, and is returned as it is.
+ * The status word is read after the work already enqueued on `stream` (this
+ * synchronizes `stream`), then cleared on `stream`.
  *   ws:          a workspace from dvl_workspace_init.
  *   status_bits: HOST (out).
  * Errors: DVL_ERR_INVALID_ARG, DVL_ERR_CUDA. */
@@ -213,19 +220,32 @@ dvl_status dvl_draft_plan(const dvl_head *head, int32_t M, int32_t k, const char
  * library's own device memory (a static __device__ array: every GPU that
  * loads the library keeps it until the process exits).  This entry point
  * allocates nothing and frees nothing.
- *   Same arguments, arithmetic, results and errors as dvl_draft_argmax,
- *   without ws / ws_bytes.  M above DVL_MAX_M (32), the most the fixed
- *   scratch holds, returns DVL_ERR_INVALID_ARG before anything is enqueued.
- *   The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, once per device, with that device current); make
- *   that first call before any stream capture.
- *   Every call clears the scratch with a memset enqueued on `stream`, then
- *   runs the argmax on it.  All calls on a device share the one array: two
- *   calls that may run at the same time on the GPU (on different streams, or
- *   from different threads) race on it and may return wrong results.  Keep
- *   them in one stream order. */
+ *   Same arguments, arithmetic and results as dvl_draft_argmax, without
+ *   ws / ws_bytes; the same argument errors.  M above DVL_MAX_M (32), the
+ *   most the fixed scratch holds, returns DVL_ERR_INVALID_ARG before
+ *   anything is enqueued.
+ *   The first call in a CUDA context looks up the array's device address
+ *   (cudaGetSymbolAddress, with that context's device current) and keeps it
+ *   for that context; make that first call before any stream capture.
+ *   Every call clears the scratch's reduction state (ticket and best keys)
+ *   with memsets enqueued on `stream`, then runs the argmax on it.  The
+ *   scratch's status word is not cleared: device-side failures (the bits of
+ *   dvl_workspace_status) accumulate there until dvl_noalloc_status reads
+ *   them.  All calls on a device share the one array: two calls that may
+ *   run at the same time on the GPU (on different streams, or from
+ *   different threads) race on it and may return wrong results.  Keep them
+ *   in one stream order. */
 dvl_status dvl_draft_argmax_noalloc(const dvl_head *head, const void *h, int32_t M,
                                     int32_t *ids, float *max_logit, void *stream);
+
+/* The device-side failure bits that dvl_draft_argmax_noalloc calls on the
+ * current device recorded since the last read (the bits and meaning of
+ * dvl_workspace_status), read after the work already enqueued on `stream`
+ * (this synchronizes `stream`) and then cleared on `stream`.  No
+ * counterpart on the pages; allocates nothing.
+ *   status_bits: HOST (out).
+ * Errors: DVL_ERR_INVALID_ARG, DVL_ERR_CUDA. */
+dvl_status dvl_noalloc_status(uint32_t *status_bits, void *stream);
 
 /* Candidate scores through a head ("Masked MTP drafts", section "Update
  * (November 2026)": a drafter that carries no head of its own scores its
@@ -323,6 +343,36 @@ dvl_status dvl_quantize_head(const dvl_head *src, int32_t dtype, void *codes, ui
  * DVL_ERR_CUDA. */
 dvl_status dvl_learn_rows(const dvl_head *full, const int32_t *ids, int32_t n, int32_t row0,
                           void *w_trim, uint8_t *scales_trim, int32_t *d2t, void *stream);
+
+/* The whole repair step of a shortlist that learns while serving ("Masked
+ * MTP drafts", section "Update (November 2026)": the ids a static trim
+ * missed, learned into spare head rows): given the ids the target emitted,
+ * pick those the list does not hold -- each id's first occurrence, in the
+ * order given, while spare rows remain -- and copy them in as
+ * dvl_learn_rows does, into rows *n_rows, *n_rows + 1, ...
+ *   full:     the full head: N == V, d2t == NULL, id_base == 0.
+ *   ids:      HOST int32 [n], each in [0, V), in any order, repeats allowed
+ *             (n may be 0).
+ *   row_of:   HOST int32 [V] (in/out): the trimmed row that holds id t, or
+ *             -1 for an id the list lacks; learned ids get their rows.
+ *   n_rows:   HOST (in/out): rows in use; the first spare row.
+ *   capacity: rows the trimmed buffers hold (>= *n_rows).
+ *   w_trim, scales_trim (NVFP4; NULL otherwise), d2t: the trimmed head's
+ *             device buffers from row 0, sized for `capacity` rows.
+ *   learned:  HOST int32 [n] (out): the ids learned, in row order; also the
+ *             source of the d2t copy, read before the call returns.
+ *   n_learned: HOST (out): how many.
+ * Nothing is enqueued when nothing is learned.  Ordering as for
+ * dvl_learn_rows: the first reducing call after a learn on that stream
+ * must not set DVL_HEAD_STATIC on the trimmed head.  The host work is
+ * O(n); nothing is allocated.
+ * Errors: DVL_ERR_INVALID_ARG, DVL_ERR_OUT_OF_RANGE (an id outside [0, V):
+ * nothing changed, nothing enqueued), DVL_ERR_CUDA (row_of and *n_rows
+ * unchanged). */
+dvl_status dvl_learn_missing(const dvl_head *full, const int32_t *ids, int32_t n,
+                             int32_t *row_of, int32_t *n_rows, int32_t capacity, void *w_trim,
+                             uint8_t *scales_trim, int32_t *d2t, int32_t *learned,
+                             int32_t *n_learned, void *stream);
 
 /* ---------------------------------------------------------------------- */
 /* Host-only ranks builder (no GPU involved)                              */

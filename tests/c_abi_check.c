@@ -1,7 +1,8 @@
 /* A C11 program against include/dvl.h: the header is plain C and the
  * library's host entry points work without C++ or Python.  It calls only
- * functions that need no GPU (the ranks builder, the constants, and the
- * argument checks, which fail before anything is enqueued) and prints
+ * functions that need no GPU (the ranks builder, the constants, the
+ * argument checks, which fail before anything is enqueued, and the repair
+ * step's selection where it selects nothing to copy) and prints
  * "c abi ok". */
 #include <stdint.h>
 #include <stdio.h>
@@ -58,6 +59,33 @@ int main(void)
                         (const int32_t *)(uintptr_t)0x2000, 4, logit, NULL) == DVL_ERR_INVALID_ARG);
     uint32_t bits = 0;
     CHECK(dvl_workspace_status(NULL, &bits, NULL) == DVL_ERR_INVALID_ARG);
+    CHECK(dvl_noalloc_status(NULL, NULL) == DVL_ERR_INVALID_ARG);
+
+    /* the repair step: ids already in the list, or no spare row left, copy
+     * nothing (so nothing is enqueued and no GPU is needed) */
+    head.dtype = DVL_BF16;
+    int32_t row_of[100];
+    for (int i = 0; i < 100; ++i)
+        row_of[i] = -1;
+    row_of[5] = 0;
+    row_of[9] = 1;
+    int32_t rows = 2, learned[4], nl = -1;
+    const int32_t present[] = {9, 5, 9};
+    void *wt = (void *)(uintptr_t)0x1000;
+    int32_t *d2t = (int32_t *)(uintptr_t)0x2000;
+    CHECK(dvl_learn_missing(&head, present, 3, row_of, &rows, 8, wt, NULL, d2t, learned, &nl,
+                            NULL) == DVL_OK);
+    CHECK(nl == 0 && rows == 2);
+    const int32_t fresh[] = {7, 7, 3};
+    CHECK(dvl_learn_missing(&head, fresh, 3, row_of, &rows, 2, wt, NULL, d2t, learned, &nl,
+                            NULL) == DVL_OK);
+    CHECK(nl == 0 && rows == 2 && row_of[7] == -1 && row_of[3] == -1);
+    const int32_t outside[] = {7, 100};
+    CHECK(dvl_learn_missing(&head, outside, 2, row_of, &rows, 8, wt, NULL, d2t, learned, &nl,
+                            NULL) == DVL_ERR_OUT_OF_RANGE);
+    CHECK(row_of[7] == -1 && rows == 2);
+    CHECK(dvl_learn_missing(&head, fresh, 3, row_of, &rows, 1, wt, NULL, d2t, learned, &nl,
+                            NULL) == DVL_ERR_INVALID_ARG); /* capacity below the rows in use */
     printf("c abi ok\n");
     return 0;
 }

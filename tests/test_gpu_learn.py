@@ -118,3 +118,27 @@ def test_learn_and_draft_in_a_loop_without_syncs(dvl, oracle_mod):
     for (ids, vals, n), h in zip(outs, hs):
         L, _ = oracle_mod.logits_bf16(wb[active[:n]], h)
         check_argmax(oracle_mod, L, active[:n], ids.cpu().numpy(), vals.cpu().numpy())
+
+
+def test_heads_handed_out_before_the_next_draft_are_not_static(dvl, oracle_mod):
+    # every head taken between a learn and the first draft call enqueued
+    # after it streams nothing before its wait; once such a call is
+    # enqueued, later heads may
+    V, K, M = 4000, 256, 1
+    wb = S.normal_bf16_rows(90, V, K, 0.02)
+    h = S.hidden_bf16(91, M, K)
+    ranks = np.arange(0, V, 7, dtype=np.int32)
+    sl = dvl.Shortlist(dev(wb), ranks, capacity=len(ranks) + 8)
+    a, b = sl.head(), sl.head()
+    assert not a.static and not b.static
+    dvl.draft_argmax(b, dev(h))
+    assert sl.head().static
+    assert sl.learn([1, 2, 1, 7]).tolist() == [1, 2]  # 7 is in the list already
+    c, d = sl.head(), sl.head()
+    assert not c.static and not d.static
+    ids, vals = dvl.draft_argmax(d, dev(h))
+    assert sl.head().static
+    active = sl.d2t[:sl.n].cpu().numpy()
+    L, _ = oracle_mod.logits_bf16(wb[active], h)
+    check_argmax(oracle_mod, L, active, ids.cpu().numpy(), vals.cpu().numpy())
+    assert sl.row_of[1] == len(ranks) and sl.row_of[2] == len(ranks) + 1

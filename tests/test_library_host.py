@@ -196,6 +196,38 @@ def test_learn_checks_reject_before_any_launch(dvl):
     assert L.dvl_learn_rows(ctypes.byref(nv), ok, 2, 0, 0x1000, None, 0x2000, None) == 1
 
 
+def test_learn_missing_selects_on_the_host(dvl):
+    # the repair step's decision: ids the list holds, repeats and ids past
+    # the capacity are not learned; a call that learns nothing enqueues
+    # nothing (so this runs without a GPU); an id outside [0, V) changes
+    # nothing
+    from draft_vocab_lm_gb300._native import lib
+    L = lib()
+    h = _head()
+    row_of = np.full(100, -1, dtype=np.int32)
+    row_of[[4, 7, 50]] = [0, 1, 2]
+    learned = np.zeros(8, dtype=np.int32)
+    rows, nl = ctypes.c_int32(3), ctypes.c_int32(-1)
+
+    def call(ids, cap):
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        return L.dvl_learn_missing(ctypes.byref(h), ids.ctypes.data if ids.size else None,
+                                   ids.size, row_of.ctypes.data, ctypes.byref(rows), cap,
+                                   0x1000, None, 0x2000, learned.ctypes.data, ctypes.byref(nl),
+                                   None)
+    assert call([7, 4, 50, 7], 10) == 0 and nl.value == 0 and rows.value == 3
+    assert call([], 10) == 0 and nl.value == 0
+    assert call([8, 8, 9], 3) == 0 and nl.value == 0 and rows.value == 3  # no spare row
+    before = row_of.copy()
+    assert call([8, 100], 10) == 2 and rows.value == 3  # 100 is outside [0, V)
+    assert np.array_equal(row_of, before)
+    assert call([8], 2) == 1  # capacity below the rows in use
+    nv = _head(dtype=1, scales=None)
+    assert L.dvl_learn_missing(ctypes.byref(nv), None, 0, row_of.ctypes.data, ctypes.byref(rows),
+                               10, 0x1000, None, 0x2000, learned.ctypes.data, ctypes.byref(nl),
+                               None) == 1
+
+
 def test_fp8_head_checks(dvl):
     # FP8 heads take no per-block scales; a valid FP8 head passes the head
     # checks (the out-of-range id is what a trim then refuses)
