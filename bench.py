@@ -473,6 +473,8 @@ def run_ours(args):
         cpu_val, threads, sample, _ = oracle_rate(5.0, wl2)
         line["cpu_baseline"] = {"value": round(cpu_val, 4), "unit": "calls/s", "cores": threads,
                                 "kind": "oracle", "sample": sample}
+    if "detail" in line:
+        line["targets"] = targets(line["detail"])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -559,6 +561,15 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
                                                        ws=ws), n_calls, R)
     out["c1_shortlist16k_M3_argmax"] = entry(RL.call_bytes(wl1.N, wl1.K, 3), *t, peak,
                                              {"l2_rotation_copies": R1})
+    gsl3 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gsl3):
+        for i in range(50):
+            dvl.draft_argmax(heads[i % R1], h3s, ids=ids, logits=lg, ws=ws)
+    t = repeat_stats(torch, lambda i: gsl3.replay(), 4, R)
+    out["c1_shortlist16k_M3_argmax_graph50"] = entry(RL.call_bytes(wl1.N, wl1.K, 3), t[0] / 50,
+                                                     t[1] / 50, t[2] / 50, peak,
+                                                     {"l2_rotation_copies": R1})
+    del gsl3
     t_hot = repeat_stats(torch, lambda i: dvl.draft_argmax(heads[0], h1s, ids=ids, logits=lg,
                                                            ws=ws), n_calls, R)
     out["c1_shortlist16k_M1_argmax_l2hot"] = entry(b1, *t_hot, peak, {"note": "L2-hot, same copy"})
@@ -654,6 +665,32 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
                 "248,320-row head of the same width",
     }
     return out
+
+
+def targets(d):
+    """The bandwidth goal's workloads in one compact object (bf16 full
+    vocabulary and 16k shortlist at M = 1 and 3; the 32k trim at M = 3, 4):
+    microseconds per call, GB/s and the fractions of the measured and the
+    nominal 8 TB/s peak, eager and, where timed, CUDA-graph replay."""
+    def pick(key, gkey=None):
+        e = d.get(key)
+        if not e:
+            return None
+        o = {"us": e["us_per_call"], "GBs": e["GBs"], "of_meas": e["frac_of_measured_hbm"],
+             "of_8TBs": e["frac_of_nominal_8TBs"]}
+        g = d.get(gkey) if gkey else None
+        if g:
+            o.update({"us_graph": g["us_per_call"], "GBs_graph": g["GBs"],
+                      "of_8TBs_graph": g["frac_of_nominal_8TBs"]})
+        return o
+    return {
+        "c1_m1": pick("c1_shortlist16k_M1_argmax", "c1_shortlist16k_M1_argmax_graph50"),
+        "c1_m3": pick("c1_shortlist16k_M3_argmax", "c1_shortlist16k_M3_argmax_graph50"),
+        "c2_m1": pick("c2_full_M1_argmax", "c2_full_M1_argmax_graph50"),
+        "c2_m3": pick("c2_full_M3_argmax"),
+        "c3_m3": pick("c3_trim32k_K5120_M3_argmax"),
+        "c3_m4": pick("c3_trim32k_K5120_M4_argmax"),
+    }
 
 
 def main():
