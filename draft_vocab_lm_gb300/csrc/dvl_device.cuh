@@ -129,6 +129,23 @@ __device__ __forceinline__ void list_insert_smem(uint64_t *lst, uint64_t key)
         lst[i] = t.v[i];
 }
 
+// The cross-block ticket: a wrapping increment (atomicInc semantics) with
+// release and acquire at GPU scope.  Release: the calling block's earlier
+// writes (made before a __syncthreads, by any of its threads) are visible
+// to whoever observes the increment; acquire: the caller's later reads (and,
+// after a __syncthreads, its block's) see what every earlier incrementer
+// released.  One round trip, where a full fence on each side costs far more
+// while the next kernel's loads crowd the memory system.
+__device__ __forceinline__ unsigned int ticket_inc(unsigned int *p, unsigned int lim)
+{
+    unsigned int old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(lim)
+                 : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t x)
 {
 #pragma unroll
@@ -248,16 +265,14 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
                     slots[((size_t)m * gridDim.x + blockIdx.x) * KM + i] = L.v[i];
         }
     }
-    __threadfence();  // this thread's slot stores before the ticket
-    __syncthreads();
+    __syncthreads();  // the block's keys and slots, then its ticket (release)
     if (threadIdx.x == 0) {
-        unsigned int prev = atomicInc(ticket, gridDim.x - 1);
+        unsigned int prev = ticket_inc(ticket, gridDim.x - 1);
         s_last = (prev == gridDim.x - 1);
     }
-    __syncthreads();
+    __syncthreads();  // the last block's reads follow its acquire
     if (!s_last)
         return;
-    __threadfence();
     if constexpr (KM == 1) {
         // one thread per hidden row: the swaps go out together
         for (int m = threadIdx.x; m < M; m += blockDim.x) {
