@@ -642,6 +642,13 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
                                                            ws=ws), n_calls, R)
         out[f"c5_nvfp4_32k_K5120_M{M}_argmax"] = entry(
             RL.call_bytes(wl5.N, wl5.K, M, dtype="nvfp4"), *t, peak, {"l2_rotation_copies": R5})
+    # batched drafting on the same head: 16 hidden rows in one pass
+    hh = dev(torch, S.hidden_bf16(516, 16, wl5.K))
+    t = repeat_stats(torch, lambda i: dvl.draft_argmax(hs[i % R5], hh, ids=ids, logits=lg,
+                                                       ws=ws), n_calls, R)
+    out["c5_nvfp4_32k_K5120_M16_argmax"] = entry(
+        RL.call_bytes(wl5.N, wl5.K, 16, dtype="nvfp4"), *t, peak,
+        {"l2_rotation_copies": R5, "launches": dvl.draft_plan(hs[0], 16)[1]})
     del hs
     # FP8 (E4M3, one tensor scale) full-vocabulary head, 248,320 x 2,560:
     # the same rows as c2 at half the bytes
@@ -655,6 +662,12 @@ def detail(torch, dvl, args, wl2, head2, ws, ids, lg, peak, l2):
     t = repeat_stats(torch, lambda i: dvl.draft_topk(head8, h1, 4, ids=ids, logits=lg, ws=ws),
                      n_calls, R)
     out["fp8_full_M1_top4"] = entry(RL.call_bytes(N2, K2, 1, dtype="fp8", k=4), *t, peak)
+    # batched drafting, 8 streams x 4 draft slots: 32 hidden rows in one pass
+    h32 = dev(torch, S.hidden_bf16(532, 32, K2))
+    t = repeat_stats(torch, lambda i: dvl.draft_argmax(head8, h32, ids=ids, logits=lg, ws=ws),
+                     50, R)
+    out["fp8_full_M32_argmax"] = entry(RL.call_bytes(N2, K2, 32, dtype="fp8"), *t, peak,
+                                       {"launches": dvl.draft_plan(head8, 32)[1]})
     del head8
     # trim vs full at M = 1 (same run)
     full = out["c2_full_M1_argmax"]["us_per_call"]

@@ -49,7 +49,7 @@
 namespace dvl {
 namespace lowbit {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;  // threads per block when two blocks fit per SM
 constexpr int kWarps = kThreads / 32;
 constexpr int kRows = 16;      // head rows per warp group (MMA M)
 constexpr int kChunk = 128;    // weights per row per k chunk
@@ -63,11 +63,24 @@ template <int FMT> __host__ __device__ constexpr int chunk_bytes() { return FMT 
 template <int FMT, int M, int KC, int KM>
 __host__ __device__ constexpr int ring_depth()
 {
-    // FP8 argmax with four hidden rows at 5,120 spills registers with a
-    // 4-deep ring (ptxas); a 2-deep one keeps it within 128
-    return (FMT == kFmtFp8 && M >= 4 && KC == 5120 && KM == 1) ? 2 : 4;
+    // FP8 argmax from four hidden rows on spills registers with a 4-deep
+    // ring (ptxas), a 2-deep one keeps it within 128; FP8 top-k above 8 rows
+    // (lists in shared memory) affords 5, measured 27% faster than 2
+    if (M > 8)
+        return FMT == kFmtFp8 ? (KM == 1 ? 2 : 5) : 4;
+    return (FMT == kFmtFp8 && M >= 4 && KM == 1) ? 2 : 4;
 }
 constexpr int kLists = kWarps * 8;  // candidate lists per hidden row (8 row pairs per warp)
+
+// Hidden rows are the MMA's n8 columns: ceil(M / 8) groups of 8, each an
+// MMA of its own against the same decoded head fragment.
+template <int M> __host__ __device__ constexpr int n_groups() { return (M + 7) / 8; }
+// Threads per block: 256 (two blocks per SM) unless the staged hidden rows
+// (M x K f16) leave room for one block per SM only; then one block of 512.
+template <int M, int KC> __host__ __device__ constexpr int block_threads()
+{
+    return (size_t)M * KC * 2 > 96 * 1024 ? 512 : 256;
+}
 
 // Four bytes of codes -> four f16x2 (byte t: low nibble in the low half).
 __device__ __forceinline__ void e2m1_word(uint32_t w, uint32_t (&f)[4])
@@ -133,8 +146,14 @@ __host__ __device__ inline size_t lowbit_h_bytes(int Kpad, int M) { return (size
 
 // K == KC (a multiple of 128) when KC > 0; K read from the arguments when 0.
 template <int FMT, int M, int KM, int KC>
-__global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const ArgmaxArgs a)
+__global__ void __launch_bounds__(block_threads<M, KC>(), 512 / block_threads<M, KC>())
+    argmax_lowbit_kernel(const ArgmaxArgs a)
 {
+    constexpr int TH = block_threads<M, KC>(), NW = TH / 32, NL = NW * 8;
+    constexpr int NG = n_groups<M>();
+    // hidden rows of this launch: M itself up to 8; the instantiations for
+    // 16 and 32 take any count up to that from a.m_rows
+    const int MR = M > 8 ? a.m_rows : M;
     constexpr int kNB = ring_depth<FMT, M, KC, KM>(), kQW = q_words<FMT>();
     constexpr bool kNv = FMT == kFmtNvfp4;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -142,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
     const int Kpad = KC > 0 ? KC : a.Kpad, C = Kpad / kChunk;
     uint4 *s_h = reinterpret_cast<uint4 *>(smem);
     uint64_t *s_cand = reinterpret_cast<uint64_t *>(smem + lowbit_h_bytes(Kpad, M));
-    __shared__ unsigned int s_wmax[kWarps];
+    __shared__ unsigned int s_wmax[NW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -154,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
 
     // This warp's rows: one balanced contiguous range per warp of the grid,
     // walked 16 rows (one MMA tile) at a time; the last group may be partial.
-    const long long GW = (long long)gridDim.x * kWarps;
-    const long long gw = (long long)blockIdx.x * kWarps + warp;
+    const long long GW = (long long)gridDim.x * NW;
+    const long long gw = (long long)blockIdx.x * NW + warp;
     const int row0 = (int)((long long)a.N * gw / GW);
     const int rend = (int)((long long)a.N * (gw + 1) / GW);
     const int my_groups = (rend - row0 + kRows - 1) / kRows;
@@ -241,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
     auto read_max = [&]() {
         unsigned int mx = 0u;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w)
+        for (int w = 0; w < NW; ++w)
             mx = max(mx, s_wmax[w]);
         return mx;
     };
@@ -252,24 +271,66 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
         const int u = (r / M) & 3, c = r / (M * 4);
         return kChunk * c + 32 * qq + 8 * u;
     };
+    // unit i of h in h's own order (row gg, elements e .. e + 8) -> its slot
+    // in the [chunk][u][g][q] layout (compile-time width)
+    auto natural_unit = [](int i, int &gg, int &slot) {
+        constexpr int kU = (KC > 0 ? KC : 8) / 8;  // units per row (used with KC > 0)
+        gg = i / kU;
+        const int e = 8 * (i - gg * kU);
+        const int c = e / kChunk, r = e - c * kChunk;
+        slot = ((c * 4 + ((r & 31) >> 3)) * M + gg) * 4 + (r >> 5);
+        return e;
+    };
     int shift;
-    for (int i = tid; i < M * kLists * KM; i += kThreads)
+    for (int i = tid; i < M * NL * KM; i += TH)
         s_cand[i] = 0ull;
-    if constexpr (KC > 0) {
-        // one pass: every unit loaded once, its maximum taken, then stored
+    if constexpr (KC > 0 && NG > 1) {
+        // many hidden rows: the raw units go straight to shared memory
+        // (cp.async, no registers, which the load ring holds; rows past MR
+        // zero-filled), read in h's own order so that a warp reads 512
+        // contiguous bytes, each placed at its unit's slot; the maximum is
+        // read back from there, and each thread converts its units in place
         constexpr int kUnits = (KC / kChunk) * 16 * M;
-        constexpr int kPer = (kUnits + kThreads - 1) / kThreads;
+        for (int i = tid; i < kUnits; i += TH) {
+            int gg, slot;
+            const int e = natural_unit(i, gg, slot);
+            const bool in = gg < MR;
+            const void *src = in ? static_cast<const void *>(a.h + (size_t)gg * KC + e)
+                                 : static_cast<const void *>(a.h);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                             static_cast<unsigned>(__cvta_generic_to_shared(s_h + slot))),
+                         "l"(src), "r"(in ? 16 : 0)
+                         : "memory");
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();  // units land in other threads' slots
+        unsigned int mx = 0u;
+        for (int i = tid; i < kUnits; i += TH) {
+            const uint4 x = s_h[i];
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                mx = max(mx, max(xs[t] & 0x7fffu, (xs[t] >> 16) & 0x7fffu));
+        }
+        block_max(mx);
+        __syncthreads();
+        shift = shift_of(read_max());
+        const float up = shift >= 0 ? pow2f(min(shift, 127)) : pow2f(max(shift, -126));
+        for (int i = tid; i < kUnits; i += TH)
+            s_h[i] = to_f16(s_h[i], up);  // this thread's own unit
+    } else if constexpr (KC > 0) {
+        // one pass: every unit loaded once (in h's own order, so a warp reads
+        // 512 contiguous bytes), its maximum taken, then stored to its slot
+        constexpr int kUnits = (KC / kChunk) * 16 * M;
+        constexpr int kPer = (kUnits + TH - 1) / TH;
         uint4 hx[kPer];
         unsigned int mx = 0u;
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
-            const int i = tid + j * kThreads;
+            const int i = tid + j * TH;
             hx[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (i < kUnits) {
-                int gg;
-                const int k0 = unit_k0(i, gg);
-                hx[j] = __ldg(reinterpret_cast<const uint4 *>(a.h + (size_t)gg * KC + k0));
-            }
+            if (i < kUnits)
+                hx[j] = __ldg(reinterpret_cast<const uint4 *>(a.h) + i);  // h is [M][KC]
         }
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
@@ -284,14 +345,17 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
         const float up = shift >= 0 ? pow2f(min(shift, 127)) : pow2f(max(shift, -126));
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
-            const int i = tid + j * kThreads;
-            if (i < kUnits)
-                s_h[i] = to_f16(hx[j], up);
+            const int i = tid + j * TH;
+            if (i < kUnits) {
+                int gg, slot;
+                natural_unit(i, gg, slot);
+                s_h[slot] = to_f16(hx[j], up);
+            }
         }
     } else {
         // two passes over h from L2: the maximum, then the staging
         unsigned int mx = 0u;
-        for (int i = tid; i < M * K / 2; i += kThreads) {
+        for (int i = tid; i < M * K / 2; i += TH) {
             const uint32_t x = __ldg(reinterpret_cast<const uint32_t *>(a.h) + i);
             mx = max(mx, max(x & 0x7fffu, (x >> 16) & 0x7fffu));
         }
@@ -300,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
         shift = shift_of(read_max());
         const float up = shift >= 0 ? pow2f(min(shift, 127)) : pow2f(max(shift, -126));
         const int nunits = C * 4 * M * 4;
-        for (int i = tid; i < nunits; i += kThreads) {
+        for (int i = tid; i < nunits; i += TH) {
             int gg;
             const int k0 = unit_k0(i, gg);
             uint4 x = make_uint4(0u, 0u, 0u, 0u);
@@ -314,42 +378,104 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
         prologue();
     const float down = (shift >= 0 ? pow2f(max(-shift, -126)) : pow2f(min(-shift, 127))) * a.gscale;
 
-    // argmax: the best key of hidden rows 2q and 2q + 1 in registers; top-k:
-    // the lists in this lane's own candidate slots in shared memory (zeroed
-    // above), which the block merge reads at the end
-    TopList<1> best0, best1;
-    best0.init();
-    best1.init();
+    // argmax: the best key of hidden rows 8G + 2q and 8G + 2q + 1 (group G)
+    // in registers; top-k: the lists in this lane's own candidate slots in
+    // shared memory (zeroed above), which the block merge reads at the end
+    // (more than one group: the argmax keys live in the shared-memory lists
+    // too, which frees the registers)
+    constexpr bool kRegBest = KM == 1 && NG == 1;
+    TopList<1> best[kRegBest ? 1 : 1][2];
+    best[0][0].init();
+    best[0][1].init();
     const int slot = warp * 8 + g;
-    uint64_t *list0 = s_cand + ((size_t)(2 * q) * kLists + slot) * KM;
-    uint64_t *list1 = s_cand + ((size_t)(2 * q + 1) * kLists + slot) * KM;
-    auto keep0 = [&](uint64_t key) {
-        if constexpr (KM == 1)
-            best0.insert(key);
+    auto list_of = [&](int m) { return s_cand + ((size_t)m * NL + slot) * KM; };
+    auto keep = [&](int G, int s, uint64_t key) {
+        if constexpr (kRegBest)
+            best[0][s].insert(key);
         else
-            list_insert_smem<KM>(list0, key);
+            list_insert_smem<KM>(list_of(8 * G + 2 * q + s), key);
     };
-    auto keep1 = [&](uint64_t key) {
-        if constexpr (KM == 1)
-            best1.insert(key);
-        else
-            list_insert_smem<KM>(list1, key);
-    };
-    // four independent accumulators, so consecutive MMAs do not wait on
-    // each other; summed at the end of a group
-    float acc[4][4];
+    // independent accumulator chains (four for one group of hidden rows, two
+    // or one per group for more), so consecutive MMAs do not wait on each
+    // other; summed at the end of a row group
+    constexpr int CH = NG == 1 ? 4 : (NG == 2 ? 2 : 1);
+    float acc[NG][CH][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int G = 0; G < NG; ++G)
+#pragma unroll
+        for (int i = 0; i < CH; ++i)
+            acc[G][i][0] = acc[G][i][1] = acc[G][i][2] = acc[G][i][3] = 0.f;
     // B fragments: lanes whose MMA column g >= M keep zeros throughout
     uint32_t hw[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j)
         hw[j] = 0u;
 
+    // One 128-wide k chunk of rows ra (codes qa, scales sa) and rb, against
+    // two or more groups of hidden rows: each 16-byte unit of h (pairs 4u ..
+    // 4u + 3, i.e. MMAs 2u and 2u + 1) is read per group just before use.
+    auto chunk_groups = [&](const uint4 (&qa)[kQW], const uint4 (&qb)[kQW], uint32_t sa,
+                            uint32_t sb, int cidx) {
+        const uint4 *hp0 = s_h + (size_t)cidx * (16 * M) + q;
+        auto hunit = [&](int G, int u) {
+            const int gg = 8 * G + g;
+            return gg < M ? hp0[u * 4 * M + gg * 4] : make_uint4(0u, 0u, 0u, 0u);
+        };
+        if constexpr (!kNv) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                uint32_t af[2][4];  // A fragments of MMAs 2u and 2u + 1
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int t = 2 * u + h2;
+                    const uint4 &xa = qa[t >> 2], &xb = qb[t >> 2];
+                    const uint32_t wa = (t & 3) == 0 ? xa.x : (t & 3) == 1 ? xa.y : (t & 3) == 2 ? xa.z : xa.w;
+                    const uint32_t wb = (t & 3) == 0 ? xb.x : (t & 3) == 1 ? xb.y : (t & 3) == 2 ? xb.z : xb.w;
+                    e4m3_word(wa, af[h2][0], af[h2][2]);
+                    e4m3_word(wb, af[h2][1], af[h2][3]);
+                }
+#pragma unroll
+                for (int G = 0; G < NG; ++G) {
+                    const uint4 v = hunit(G, u);
+                    mma_f16(acc[G][(2 * u) % CH], af[0][0], af[0][1], af[0][2], af[0][3], v.x, v.y);
+                    mma_f16(acc[G][(2 * u + 1) % CH], af[1][0], af[1][1], af[1][2], af[1][3], v.z,
+                            v.w);
+                }
+            }
+            return;
+        }
+        // NVFP4: code word u of each row holds pairs 4u .. 4u + 3 (MMAs 2u
+        // and 2u + 1); it is decoded and scaled just before its MMAs
+        uint32_t sa_lo, sa_hi, sb_lo, sb_hi;
+        e4m3_pair(sa, sa_lo, sa_hi);
+        e4m3_pair(sb, sb_lo, sb_hi);
+        const uint32_t wa[4] = {qa[0].x, qa[0].y, qa[0].z, qa[0].w};
+        const uint32_t wb[4] = {qb[0].x, qb[0].y, qb[0].z, qb[0].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            uint32_t fa[4], fb[4];
+            e2m1_word(wa[u], fa);
+            e2m1_word(wb[u], fb);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                fa[i] = hmul2(fa[i], u < 2 ? sa_lo : sa_hi);
+                fb[i] = hmul2(fb[i], u < 2 ? sb_lo : sb_hi);
+            }
+#pragma unroll
+            for (int G = 0; G < NG; ++G) {
+                const uint4 v = hunit(G, u);
+                mma_f16(acc[G][(2 * u) % CH], fa[0], fb[0], fa[1], fb[1], v.x, v.y);
+                mma_f16(acc[G][(2 * u + 1) % CH], fa[2], fb[2], fa[3], fb[3], v.z, v.w);
+            }
+        }
+    };
     // One 128-wide k chunk of rows ra (codes qa, scales sa) and rb.
     auto chunk = [&](const uint4 (&qa)[kQW], const uint4 (&qb)[kQW], uint32_t sa, uint32_t sb,
                      int cidx) {
+        if constexpr (NG > 1) {
+            chunk_groups(qa, qb, sa, sb, cidx);
+            return;
+        }
         if (g < M) {
             const uint4 *hp = s_h + (size_t)cidx * (16 * M) + (g * 4 + q);
 #pragma unroll
@@ -369,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
                 uint32_t a0, a2, a1, a3;
                 e4m3_word(wa, a0, a2);
                 e4m3_word(wb, a1, a3);
-                mma_f16(acc[t & 3], a0, a1, a2, a3, hw[2 * t], hw[2 * t + 1]);
+                mma_f16(acc[0][t & 3], a0, a1, a2, a3, hw[2 * t], hw[2 * t + 1]);
             }
             return;
         }
@@ -398,29 +524,41 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
         }
 #pragma unroll
         for (int t = 0; t < 8; ++t)
-            mma_f16(acc[t & 3], fa[2 * t], fb[2 * t], fa[2 * t + 1], fb[2 * t + 1], hw[2 * t],
+            mma_f16(acc[0][t & 3], fa[2 * t], fb[2 * t], fa[2 * t + 1], fb[2 * t + 1], hw[2 * t],
                     hw[2 * t + 1]);
     };
-    // Rows ra (c0, c1) and rb (c2, c3) of a finished group; hidden rows 2q, 2q + 1.
+    // Rows ra (c0, c1) and rb (c2, c3) of a finished row group; hidden rows
+    // 8G + 2q, 8G + 2q + 1 of each group G.
     auto finish_group = [&](int ra, int ida, int idb) {
         const int rb = ra + 8;
-        float d[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            d[j] = (acc[0][j] + acc[1][j]) + (acc[2][j] + acc[3][j]);
-            acc[0][j] = acc[1][j] = acc[2][j] = acc[3][j] = 0.f;
-        }
-        if (ra < rend) {
-            if (2 * q < M)
-                keep0(make_key(d[0] * down, ida));
-            if (2 * q + 1 < M)
-                keep1(make_key(d[1] * down, ida));
-        }
-        if (rb < rend) {
-            if (2 * q < M)
-                keep0(make_key(d[2] * down, idb));
-            if (2 * q + 1 < M)
-                keep1(make_key(d[3] * down, idb));
+        for (int G = 0; G < NG; ++G) {
+            float d[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if constexpr (CH == 4)
+                    d[j] = (acc[G][0][j] + acc[G][1][j]) + (acc[G][2][j] + acc[G][3][j]);
+                else if constexpr (CH == 2)
+                    d[j] = acc[G][0][j] + acc[G][1][j];
+                else
+                    d[j] = acc[G][0][j];
+#pragma unroll
+                for (int c = 0; c < CH; ++c)
+                    acc[G][c][j] = 0.f;
+            }
+            const int m0 = 8 * G + 2 * q;
+            if (ra < rend) {
+                if (m0 < MR)
+                    keep(G, 0, make_key(d[0] * down, ida));
+                if (m0 + 1 < MR)
+                    keep(G, 1, make_key(d[1] * down, ida));
+            }
+            if (rb < rend) {
+                if (m0 < MR)
+                    keep(G, 0, make_key(d[2] * down, idb));
+                if (m0 + 1 < MR)
+                    keep(G, 1, make_key(d[3] * down, idb));
+            }
         }
     };
     auto row_id = [&](int r) {
@@ -433,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
         static_assert(CC % kNB == 0, "the ring must divide the chunks");
         // NVFP4 unrolls the whole group; FP8 (twice the code bytes per
         // chunk) a multiple of the ring, which keeps it within the registers
-        constexpr int kCU = kNv ? CC : 2 * kNB;
+        // (more than one group of hidden rows: the same window as FP8)
+        constexpr int kCU = kNv && NG == 1 ? CC : 2 * kNB;
         for (int li = 0; li < my_groups; ++li) {
             const uint8_t *nqa, *nsa;
             bool nva, nvb;
@@ -515,43 +654,44 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_lowbit_kernel(const Argmax
         }
     }
 
-    if constexpr (KM == 1) {
-        if (2 * q < M)
-            list0[0] = best0.v[0];
-        if (2 * q + 1 < M)
-            list1[0] = best1.v[0];
+    if constexpr (kRegBest) {
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2)
+            if (2 * q + s2 < MR)
+                list_of(2 * q + s2)[0] = best[0][s2].v[0];
     }
     __syncthreads();
-    block_finish<KM>(s_cand, M, kLists, a);
+    block_finish<KM>(s_cand, MR, NL, a);
 }
 
 template <int FMT, int M, int KM, int KC>
 cudaError_t launch_one(const ArgmaxArgs &a, cudaStream_t s)
 {
-    const size_t smem = lowbit_h_bytes(a.Kpad, M) + (size_t)M * kLists * KM * 8;
+    constexpr int TH = block_threads<M, KC>(), NW = TH / 32;
+    const size_t smem = lowbit_h_bytes(a.Kpad, M) + (size_t)M * (NW * 8) * KM * 8;
     DeviceInfo di;
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess)
         return e;
     auto kern = argmax_lowbit_kernel<FMT, M, KM, KC>;
     int per_sm = 0;
-    e = blocks_per_sm(reinterpret_cast<const void *>(kern), kThreads, smem, &per_sm);
+    e = blocks_per_sm(reinterpret_cast<const void *>(kern), TH, smem, &per_sm);
     if (e != cudaSuccess)
         return e;
     if (per_sm < 1)
         return cudaErrorInvalidConfiguration;
-    if (per_sm > 2)
-        per_sm = 2;
+    if (per_sm > 512 / TH)
+        per_sm = 512 / TH;
     long long grid = (long long)di.sms * per_sm;
     // at least half an MMA tile of rows per warp on average
-    const long long max_by_rows = ((long long)a.N + kWarps * 8 - 1) / (kWarps * 8);
+    const long long max_by_rows = ((long long)a.N + NW * 8 - 1) / (NW * 8);
     if (grid > max_by_rows)
         grid = max_by_rows;
     if (grid > kMaxCtas)
         grid = kMaxCtas;
     if (grid < 1)
         grid = 1;
-    return launch_pdl(kern, (unsigned)grid, kThreads, smem, s, a);
+    return launch_pdl(kern, (unsigned)grid, TH, smem, s, a);
 }
 
 inline int kpad_of(int K) { return (K + kChunk - 1) / kChunk * kChunk; }
@@ -595,6 +735,27 @@ cudaError_t launch_kc(const ArgmaxArgs &a, int M, cudaStream_t s)
     return cudaErrorInvalidValue;
 }
 
+// argmax / top-k for 9 .. 32 hidden rows in one pass at the unrolled widths:
+// instantiated for 16 and 32 rows (two and four groups of 8 MMA columns),
+// with the launch's row count in a.m_rows; rows past it stage zeros and are
+// not merged.  At 5,120 32 staged rows do not fit, nor do 32 rows of top-k
+// lists next to them at 2,560: those calls take 16 rows per launch.
+template <int FMT, int KM>
+cudaError_t launch_groups(const ArgmaxArgs &a, int M, cudaStream_t s)
+{
+    ArgmaxArgs b = a;
+    b.m_rows = M;
+    if (a.K == 2560) {
+        if (M <= 16)
+            return launch_one<FMT, 16, KM, 2560>(b, s);
+        if constexpr (KM == 1)
+            return launch_one<FMT, 32, KM, 2560>(b, s);
+    }
+    if (a.K == 5120 && M <= 16)
+        return launch_one<FMT, 16, KM, 5120>(b, s);
+    return cudaErrorInvalidValue;
+}
+
 // argmax / top-k with K read at run time, M <= 8.
 template <int FMT>
 cudaError_t launch_rt(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s)
@@ -609,6 +770,10 @@ extern template cudaError_t launch_kc<kFmtFp8, 1>(const ArgmaxArgs &, int, cudaS
 extern template cudaError_t launch_kc<kFmtNvfp4, 4>(const ArgmaxArgs &, int, cudaStream_t);
 extern template cudaError_t launch_kc<kFmtFp8, 4>(const ArgmaxArgs &, int, cudaStream_t);
 extern template cudaError_t launch_rt<kFmtNvfp4>(const ArgmaxArgs &, int, int, cudaStream_t);
+extern template cudaError_t launch_groups<kFmtNvfp4, 1>(const ArgmaxArgs &, int, cudaStream_t);
+extern template cudaError_t launch_groups<kFmtNvfp4, 4>(const ArgmaxArgs &, int, cudaStream_t);
+extern template cudaError_t launch_groups<kFmtFp8, 1>(const ArgmaxArgs &, int, cudaStream_t);
+extern template cudaError_t launch_groups<kFmtFp8, 4>(const ArgmaxArgs &, int, cudaStream_t);
 extern template cudaError_t launch_rt<kFmtFp8>(const ArgmaxArgs &, int, int, cudaStream_t);
 
 }  // namespace lowbit

@@ -145,7 +145,8 @@ dvl_status reduce_call(const dvl_head *hd, const void *h, int32_t M, int32_t k, 
     if (!ws || !aligned(ws, 16) || ws_bytes < dvl_workspace_bytes(M, k))
         return DVL_ERR_WORKSPACE;
     const int chunk =
-        hd->dtype == DVL_BF16 ? max_chunk_rows_bf16(hd->K) : max_chunk_rows_lowbit(hd->K);
+        hd->dtype == DVL_BF16 ? max_chunk_rows_bf16(hd->K)
+                              : max_chunk_rows_lowbit(hd->K, k == 1 ? 1 : DVL_MAX_TOPK);
     if (chunk < 1)
         return DVL_ERR_UNSUPPORTED;
     ArgmaxArgs a;
@@ -365,7 +366,7 @@ dvl_status dvl_draft_plan(const dvl_head *head, int32_t M, int32_t k, const char
         !launches)
         return DVL_ERR_INVALID_ARG;
     if (head->dtype != DVL_BF16) {
-        const int chunk = max_chunk_rows_lowbit(head->K);
+        const int chunk = max_chunk_rows_lowbit(head->K, k == 1 ? 1 : DVL_MAX_TOPK);
         if (chunk < 1)
             return DVL_ERR_UNSUPPORTED;
         *kernel = head->dtype == DVL_NVFP4 ? "nvfp4-mma" : "fp8-mma";

@@ -34,6 +34,8 @@ struct ArgmaxArgs {
     unsigned char *ws;        // workspace base
     bool head_static;         // w / scales / d2t not written by pending work
     int32_t V;                // vocabulary size (<= 2^31 - 1): ids lie in [0, V)
+    int32_t m_rows;           // hidden rows of this launch (kernels instantiated for a
+                              // padded count read it)
 };
 
 // Per-device facts, queried once.
@@ -69,7 +71,7 @@ cudaError_t launch_argmax_bf16_mma(const ArgmaxArgs &a, int M, int kmax, cudaStr
 // one launch.
 bool tc_argmax_supported(int M, int K);
 cudaError_t launch_argmax_tc(const ArgmaxArgs &a, int M, int kmax, cudaStream_t s);
-int max_chunk_rows_lowbit(int K);
+int max_chunk_rows_lowbit(int K, int kmax);
 
 // The argument checks of draft_argmax / draft_topk, without the workspace.
 dvl_status check_reduce_args(const dvl_head *hd, const void *h, int32_t M, int32_t k,

@@ -1,10 +1,14 @@
 """GPU parity at batched-drafting sizes where M x K exceeds 98,304 (the most a
 block could stage when every hidden row sat in shared memory at once):
 bf16 at M = 32, K = 5,120 and at M = 20, K = 24,576 (one pass on the tcgen05
-kernel, which streams tiles of h with the head), and NVFP4 / FP8 at M = 24
-and 32, K = 5,120 (chunks of 8 rows on the low-bit kernel).  Integer heads
-and hidden rows make every sum exact, so ids, logits and ties must agree
-with the oracle bit for bit; each case also checks the plan it ran on."""
+kernel, which streams tiles of h with the head), and NVFP4 / FP8 at 9 to 32
+hidden rows (one pass at K = 2,560, groups of 16 rows at 5,120, on the
+low-bit kernel with two or four groups of 8 MMA columns).  Integer heads and
+hidden rows make every sum exact, so ids, logits and ties must agree with the
+oracle bit for bit; each case also checks the plan it ran on.  Gaussian
+NVFP4 / FP8 heads of the workloads' shapes (the 32,768 x 5,120 trimmed head,
+the 248,320 x 2,560 full vocabulary) follow the parity rule at 16 and 32
+rows."""
 import numpy as np
 import pytest
 
@@ -60,10 +64,8 @@ def test_bf16_batched_one_pass(dvl, oracle_mod, N, K, M):
     exact(dvl, oracle_mod, head, L, h, M, d2t, dvl.make_workspace(M, 4))
 
 
-@pytest.mark.parametrize("fmt,N,M", [("fp8", 3001, 32), ("nvfp4", 1000, 24)])
-def test_lowbit_batched_in_chunks(dvl, oracle_mod, fmt, N, M):
-    K = 5120
-    rng = np.random.default_rng(N + M + 11)
+def lowbit_int_head(dvl, oracle_mod, fmt, N, K, M, seed):
+    rng = np.random.default_rng(seed)
     h = S.f32_to_bf16_bits(rng.integers(-3, 4, size=(M, K)).astype(np.float32))
     d2t = rng.permutation(3 * N)[:N].astype(np.int32)
     if fmt == "fp8":
@@ -76,5 +78,52 @@ def test_lowbit_batched_in_chunks(dvl, oracle_mod, fmt, N, M):
         g = 0.25
         head = dvl.Head(dev(q), scales=dev(sc), global_scale=g, V=3 * N, d2t=dev(d2t))
         L, _ = oracle_mod.logits_nvfp4(q, sc, g, h)
-    assert dvl.draft_plan(head, M, 4) == (f"{fmt}-mma", (M + 7) // 8)
+    return head, L, h, d2t
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+@pytest.mark.parametrize("K,M", [(2560, 9), (2560, 16), (2560, 17), (2560, 32),
+                                 (5120, 12), (5120, 16), (5120, 24), (5120, 32)])
+def test_lowbit_batched_one_pass(dvl, oracle_mod, fmt, K, M):
+    # one launch for up to 32 rows (argmax) at 2,560, else one per 16 rows:
+    # the head is read once per launch
+    N = 3001 if K == 2560 else 1000
+    head, L, h, d2t = lowbit_int_head(dvl, oracle_mod, fmt, N, K, M, N + K + M + 11)
+    assert dvl.draft_plan(head, M, 4) == (f"{fmt}-mma", (M + 15) // 16)
+    assert dvl.draft_plan(head, M, 1) == (f"{fmt}-mma", 1 if K == 2560 else (M + 15) // 16)
     exact(dvl, oracle_mod, head, L, h, M, d2t, dvl.make_workspace(M, 4))
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_lowbit_batched_ragged_rows_and_tiles(dvl, oracle_mod, fmt):
+    # a head whose rows end mid-tile and a few rows per warp, row counts
+    # that fill a group partly, and calls back to back on one workspace
+    ws = dvl.make_workspace(32, 4)
+    for N, M in ((37, 25), (4099, 10), (20011, 31)):
+        head, L, h, d2t = lowbit_int_head(dvl, oracle_mod, fmt, N, 2560, M, N + M)
+        exact(dvl, oracle_mod, head, L, h, M, d2t, ws)
+
+
+def test_lowbit_batched_gaussian_workload_shapes(dvl, oracle_mod):
+    from parity import check_argmax, check_topk
+    wl = S.c5(Ms=())
+    head = dvl.Head(dev(wl.q), scales=dev(wl.scales), global_scale=wl.g, V=wl.V,
+                    d2t=dev(wl.d2t), static=True)
+    q8, g8 = S.normal_fp8_rows(1, S.V_FULL, 2560, 0.02)
+    head8 = dvl.Head(dev(q8), fmt="fp8", global_scale=g8, V=S.V_FULL, static=True)
+    torch.cuda.synchronize()
+    ws = dvl.make_workspace(32, 4)
+    for hd, K, M, name in ((head, 5120, 16, "nvfp4"), (head8, 2560, 32, "fp8")):
+        h = S.hidden_bf16(600 + M, M, K)
+        if name == "nvfp4":
+            L, _ = oracle_mod.logits_nvfp4(wl.q, wl.scales, wl.g, h)
+            d2t = wl.d2t
+        else:
+            L, _ = oracle_mod.logits_fp8(q8, g8, h)
+            d2t = None
+        assert dvl.draft_plan(hd, M, 1) == (f"{name}-mma", 1)
+        ids, vals = dvl.draft_argmax(hd, dev(h), ws=ws)
+        check_argmax(oracle_mod, L, d2t, ids.cpu().numpy(), vals.cpu().numpy())
+        ids, vals = dvl.draft_topk(hd, dev(h), 4, ws=ws)
+        check_topk(oracle_mod, L, d2t, 4, ids.cpu().numpy(), vals.cpu().numpy())
+    assert dvl.workspace_status(ws) == 0
