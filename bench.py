@@ -53,8 +53,8 @@ def parse():
     p.add_argument("--profile", nargs="?", const="c2m1", default=None,
                    help="only warm-up + timed calls of one workload, for ncu captures: "
                         "c2m1 (default), c2m3, c1m1, c1m3, c3m1 .. c3m4, c4m8, c4m16, c4m32, c5m1, c5m3, "
-                        "scm16 (candidate scores, 16 rows x 32 through the c2 head), "
-                        "f8m1, f8m3 (FP8 full-vocabulary head)")
+                        "c5m16, scm16 (candidate scores, 16 rows x 32 through the c2 head), "
+                        "f8m1, f8m3, f8m32 (FP8 full-vocabulary head)")
     return p.parse_args()
 
 
