@@ -1,6 +1,8 @@
 // Instantiations of the register-path tensor-core kernel for bf16 heads
-// (argmax_bf16_mma.cuh) at 9 .. 16 hidden rows, width 2,560 (a translation
-// unit of its own so the library builds in parallel).
+// (argmax_bf16_mma.cuh) at 9 .. 16 hidden rows, width 2,560, argmax only:
+// top-k at those rows runs on tcgen05 (bf16_uses_mma) -- 53.5 against 58.9 us
+// at 16 rows on the 52,755-row head.  A translation unit of its own so the
+// library builds in parallel.
 #include "argmax_bf16_mma.cuh"
 
 namespace dvl {
@@ -10,9 +12,9 @@ template <int M>
 cudaError_t launch_rows(const ArgmaxArgs &a, int kmax, cudaStream_t s)
 {
     using namespace bf16mma;
-    if (a.K != 2560)
+    if (a.K != 2560 || kmax != 1)
         return cudaErrorInvalidValue;
-    return kmax == 1 ? launch<M, 1, 2560, 4>(a, s) : launch<M, 4, 2560, 4>(a, s);
+    return launch<M, 1, 2560, 4>(a, s);
 }
 
 }  // namespace

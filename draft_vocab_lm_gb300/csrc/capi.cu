@@ -312,7 +312,8 @@ size_t dvl_workspace_bytes(int32_t M, int32_t k)
         return 0;
     size_t b = kWsSlots;
     if (k > 1)
-        b += (size_t)kMaxCtas * (size_t)M * DVL_MAX_TOPK * sizeof(uint64_t);
+        b += (size_t)(kMaxCtas + kMaxGroups) * (size_t)M * DVL_MAX_TOPK * sizeof(uint64_t) +
+             (size_t)kMaxGroups * sizeof(uint32_t);
     return b;
 }
 

@@ -221,6 +221,103 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[P])
     }
 }
 
+// Merge, for every hidden row m < M, nl sorted lists of KM keys (list c of
+// row m at src + (m * stride + c) * KM, read from L2) into the row's KM best
+// keys, handed over as emit(m, i, key) for i < KM, best first.  Every thread
+// of the block must call it (one of its two layouts meets at a
+// __syncthreads).  A warp's lanes read consecutive lists 16 bytes at a
+// time, kBatch lists each before inserting any (one L2 round trip per
+// batch).
+template <int KM, typename Emit>
+__device__ __forceinline__ void merge_lists(const uint64_t *src, int stride, int nl, int M,
+                                            Emit emit)
+{
+    static_assert(KM % 2 == 0, "lists are read in pairs of keys");
+    constexpr int kBatch = 8;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    auto gather = [&](TopList<KM> &L, int m, int c_first, int c_step) {
+        const uint64_t *row = src + (size_t)m * stride * KM;
+        for (int c0 = c_first; c0 < nl; c0 += kBatch * c_step) {
+            ulonglong2 v[kBatch][KM / 2];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int c = c0 + u * c_step;
+#pragma unroll
+                for (int i = 0; i < KM / 2; ++i)
+                    v[u][i] = c < nl ? __ldcg(reinterpret_cast<const ulonglong2 *>(
+                                           row + (size_t)c * KM) + i)
+                                     : make_ulonglong2(0ull, 0ull);
+            }
+            // each list is sorted best first: once one of its keys loses to
+            // the current k-th best, so does the rest
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                uint64_t key[KM];
+#pragma unroll
+                for (int i = 0; i < KM / 2; ++i) {
+                    key[2 * i] = v[u][i].x;
+                    key[2 * i + 1] = v[u][i].y;
+                }
+#pragma unroll
+                for (int i = 0; i < KM; ++i) {
+                    if (key[i] <= L.v[KM - 1])
+                        break;
+                    L.insert(key[i]);
+                }
+            }
+        }
+    };
+    auto pick = [](const TopList<KM> &F, int i) {
+        uint64_t key = F.v[0];
+#pragma unroll
+        for (int j = 1; j < KM; ++j)
+            key = i == j ? F.v[j] : key;
+        return key;
+    };
+    if (M >= nwarps) {
+        // tpr threads per hidden row (a power of two, at most a warp), every
+        // row in one pass, no block-wide step
+        int tpr = 32;
+        while (tpr * M > (int)blockDim.x)
+            tpr >>= 1;
+        const int m = threadIdx.x / tpr, sub = threadIdx.x % tpr;
+        TopList<KM> L;
+        L.init();
+        if (m < M)
+            gather(L, m, sub, tpr);
+        warp_merge_topk<KM>(L, tpr);
+        if (m < M && sub < KM)
+            emit(m, sub, pick(L, sub));
+    } else {
+        // nwarps / M warps per hidden row, merged through shared memory
+        constexpr int kFinWarps = 32;  // the most warps a block can have
+        __shared__ uint64_t s_fin[kFinWarps][KM];
+        const int wpm = nwarps / M;
+        const int m = warp % M, q = warp / M;
+        TopList<KM> L;
+        L.init();
+        if (q < wpm)
+            gather(L, m, 32 * q + lane, 32 * wpm);
+        warp_merge_topk<KM>(L);
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < KM; ++i)
+                s_fin[warp][i] = q < wpm ? L.v[i] : 0ull;
+        }
+        __syncthreads();
+        if (warp < M) {
+            TopList<KM> F;  // the warps' lists are already in order
+#pragma unroll
+            for (int i = 0; i < KM; ++i)
+                F.v[i] = lane < wpm ? s_fin[warp + M * lane][i] : 0ull;
+            warp_merge_topk<KM>(F);
+            if (lane < KM)
+                emit(warp, lane, pick(F, lane));
+        }
+    }
+}
+
 // Cross-block finish of a reducing kernel.  Every block calls it once, after
 // its own candidates are final, with s_cand holding, for each of the M rows,
 // `nlists` lists of KM keys ([M][nlists][KM] in shared memory; lane l of
@@ -229,11 +326,19 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[P])
 //    atomicMax; the last block to finish swaps each key back to 0 and writes
 //    the id and the logit.
 //  - k > 1: the block's k best keys per row go to its own workspace slots
-//    ([M][blocks][k]);
-//    the last block merges every block's slots.
-// The last block is found with a wrapping ticket (atomicInc up to
-// gridDim.x - 1), so the ticket is 0 again when the call ends.  No block
-// waits for another.
+//    ([M][blocks][k]).  The last block merges every block's slots; or, when
+//    that is many lists (M * blocks >= kTwoLevelLists, and more than kGroup
+//    blocks), merging is two-level: the last block of each group of kGroup
+//    blocks (by a group ticket) merges the group's slots into the group's
+//    list, and the last of those (by the main ticket) merges the group lists
+//    -- the final merge reads blocks / kGroup lists per row, not one per
+//    block.  (Measured on the tcgen05 grid of 138 blocks: top-4 at 32 rows
+//    3.5 us faster, at 20 rows 2 us; below the threshold the extra ticket
+//    round trip costs more than it saves: +0.85 us at 8 rows on 304
+//    blocks.)
+// The last block (of a group, or of the grid) is found with a wrapping
+// ticket (an increment up to its count - 1 that wraps), so every ticket is
+// 0 again when the call ends.  No block waits for another.
 template <int KM>
 __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int nlists,
                                              const ArgmaxArgs &a)
@@ -242,7 +347,13 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
     const int nwarps = blockDim.x >> 5;
     unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws + kWsTicket);
     unsigned long long *best = reinterpret_cast<unsigned long long *>(a.ws + kWsBest);
-    unsigned long long *slots = reinterpret_cast<unsigned long long *>(a.ws + kWsSlots);
+    uint64_t *slots = reinterpret_cast<uint64_t *>(a.ws + kWsSlots);
+    // top-k: groups of kGroup blocks, their group lists and group tickets
+    // after the slots (the slot area is sized for kMaxCtas blocks)
+    const int G = (int)gridDim.x;
+    const int ngrp = (KM == 1 || M * G < kTwoLevelLists) ? 1 : (G + kGroup - 1) / kGroup;
+    uint64_t *gslots = slots + (size_t)kMaxCtas * M * KM;
+    unsigned int *gtickets = reinterpret_cast<unsigned int *>(gslots + (size_t)kMaxGroups * M * KM);
     __shared__ int s_last;
 
     for (int m = warp; m < M; m += nwarps) {
@@ -267,8 +378,16 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
     }
     __syncthreads();  // the block's keys and slots, then its ticket (release)
     if (threadIdx.x == 0) {
-        unsigned int prev = ticket_inc(ticket, gridDim.x - 1);
-        s_last = (prev == gridDim.x - 1);
+        if (ngrp == 1) {
+            const unsigned int prev = ticket_inc(ticket, (unsigned int)G - 1u);
+            s_last = (prev == (unsigned int)G - 1u);
+        } else {
+            // top-k on more than kGroup blocks: first the group's ticket
+            const int g = (int)blockIdx.x / kGroup;
+            const unsigned int gs = (unsigned int)min(kGroup, G - g * kGroup);
+            const unsigned int prev = ticket_inc(gtickets + g, gs - 1u);
+            s_last = (prev == gs - 1u);
+        }
     }
     __syncthreads();  // the last block's reads follow its acquire
     if (!s_last)
@@ -279,99 +398,30 @@ __device__ __forceinline__ void block_finish(const uint64_t *s_cand, int M, int 
             put_result(a, m, atomicExch(best + m, 0ull));
         }
     } else {
-        // The slots are [M][blocks][KM]: one hidden row's lists are
-        // contiguous, so a warp's lanes read consecutive lists, 16 bytes at
-        // a time, kBatch blocks each before inserting any (one L2 round
-        // trip per batch).
-        static_assert(KM % 2 == 0, "lists are read in pairs of keys");
-        constexpr int kBatch = 8;
-        const int G = (int)gridDim.x;
-        auto gather = [&](TopList<KM> &L, int m, int c_first, int c_step) {
-            const uint64_t *row = reinterpret_cast<const uint64_t *>(slots) + (size_t)m * G * KM;
-            for (int c0 = c_first; c0 < G; c0 += kBatch * c_step) {
-                ulonglong2 v[kBatch][KM / 2];
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    const int c = c0 + u * c_step;
-#pragma unroll
-                    for (int i = 0; i < KM / 2; ++i)
-                        v[u][i] = c < G ? __ldcg(reinterpret_cast<const ulonglong2 *>(
-                                              row + (size_t)c * KM) + i)
-                                        : make_ulonglong2(0ull, 0ull);
-                }
-                // each block's list is sorted best first: once one of its
-                // keys loses to the current k-th best, so does the rest
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    uint64_t key[KM];
-#pragma unroll
-                    for (int i = 0; i < KM / 2; ++i) {
-                        key[2 * i] = v[u][i].x;
-                        key[2 * i + 1] = v[u][i].y;
-                    }
-#pragma unroll
-                    for (int i = 0; i < KM; ++i) {
-                        if (key[i] <= L.v[KM - 1])
-                            break;
-                        L.insert(key[i]);
-                    }
-                }
-            }
+        auto emit_out = [&](int m, int i, uint64_t key) {
+            if (i < a.k)
+                put_result(a, m * a.k + i, key);
         };
-        auto write_row = [&](const TopList<KM> &F, int m) {
-            if (lane < a.k && lane < KM) {
-                uint64_t key = F.v[0];
-#pragma unroll
-                for (int i = 1; i < KM; ++i)
-                    key = lane == i ? F.v[i] : key;
-                put_result(a, m * a.k + lane, key);
-            }
-        };
-        if (M >= nwarps) {
-            // tpr threads per hidden row (a power of two, at most a warp),
-            // every row in one pass, no block-wide step
-            int tpr = 32;
-            while (tpr * M > (int)blockDim.x)
-                tpr >>= 1;
-            const int m = threadIdx.x / tpr, sub = threadIdx.x % tpr;
-            TopList<KM> L;
-            L.init();
-            if (m < M)
-                gather(L, m, sub, tpr);
-            warp_merge_topk<KM>(L, tpr);
-            if (m < M && sub < a.k && sub < KM) {
-                uint64_t key = L.v[0];
-#pragma unroll
-                for (int i = 1; i < KM; ++i)
-                    key = sub == i ? L.v[i] : key;
-                put_result(a, m * a.k + sub, key);
-            }
-        } else {
-            // nwarps / M warps per hidden row, merged through shared memory
-            constexpr int kFinWarps = 32;  // the most warps a block can have
-            __shared__ uint64_t s_fin[kFinWarps][KM];
-            const int wpm = nwarps / M;
-            const int m = warp % M, q = warp / M;
-            TopList<KM> L;
-            L.init();
-            if (q < wpm)
-                gather(L, m, 32 * q + lane, 32 * wpm);
-            warp_merge_topk<KM>(L);
-            if (lane == 0) {
-#pragma unroll
-                for (int i = 0; i < KM; ++i)
-                    s_fin[warp][i] = q < wpm ? L.v[i] : 0ull;
-            }
-            __syncthreads();
-            if (warp < M) {
-                TopList<KM> F;  // the warps' lists are already in order
-#pragma unroll
-                for (int i = 0; i < KM; ++i)
-                    F.v[i] = lane < wpm ? s_fin[warp + M * lane][i] : 0ull;
-                warp_merge_topk<KM>(F);
-                write_row(F, warp);
-            }
+        if (ngrp == 1) {
+            merge_lists<KM>(slots, G, G, M, emit_out);
+            return;
         }
+        // this block is its group's last: the group's lists -> its group list
+        const int g = (int)blockIdx.x / kGroup;
+        const int gs = min(kGroup, G - g * kGroup);
+        merge_lists<KM>(slots + (size_t)g * kGroup * KM, G, gs, M,
+                        [&](int m, int i, uint64_t key) {
+                            gslots[((size_t)m * ngrp + g) * KM + i] = key;
+                        });
+        __syncthreads();  // the group list, then the top ticket (release)
+        if (threadIdx.x == 0) {
+            const unsigned int prev = ticket_inc(ticket, (unsigned int)ngrp - 1u);
+            s_last = (prev == (unsigned int)ngrp - 1u);
+        }
+        __syncthreads();
+        if (!s_last)
+            return;
+        merge_lists<KM>(gslots, ngrp, ngrp, M, emit_out);
     }
 }
 

@@ -17,7 +17,12 @@ constexpr size_t kWsTicket = 0;           // uint32: blocks finished so far
 constexpr size_t kWsStatus = 4;           // uint32: device-side failure bits (1 << dvl_status)
 constexpr size_t kWsAmax = 8;             // uint32: a head's max |w| while it is requantized
 constexpr size_t kWsBest = 256;           // uint64[DVL_MAX_M]: best key per row (k = 1)
-constexpr size_t kWsSlots = 512;          // uint64[kMaxCtas][M][kmax] (k > 1)
+constexpr size_t kWsSlots = 512;          // uint64[M][kMaxCtas][kmax] (k > 1), then
+                                          // uint64[M][kMaxGroups][kmax] group lists and
+                                          // uint32[kMaxGroups] group tickets
+constexpr int kGroup = 16;                // top-k: blocks per first-level merge
+constexpr int kMaxGroups = kMaxCtas / kGroup;
+constexpr int kTwoLevelLists = 2560;      // top-k merges two-level from M * blocks lists
 
 // Arguments of one reducing launch (one chunk of at most 8 hidden rows).
 struct ArgmaxArgs {

@@ -127,3 +127,21 @@ def test_lowbit_batched_gaussian_workload_shapes(dvl, oracle_mod):
         ids, vals = dvl.draft_topk(hd, dev(h), 4, ws=ws)
         check_topk(oracle_mod, L, d2t, 4, ids.cpu().numpy(), vals.cpu().numpy())
     assert dvl.workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("N,M", [(40000, 32), (40000, 20), (33001, 25)])
+def test_bf16_topk_two_level_merge_bit_exact(dvl, oracle_mod, N, M):
+    # grids whose top-k merge is two-level (M x blocks >= 2,560: groups of 16
+    # blocks, the last group partial), exact integer sums with many ties
+    K = 256
+    rng = np.random.default_rng(N + M + 5)
+    w = S.f32_to_bf16_bits(rng.integers(-4, 5, size=(N, K)).astype(np.float32))
+    h = S.f32_to_bf16_bits(rng.integers(-2, 3, size=(M, K)).astype(np.float32))
+    V = 2 * N + 1
+    d2t = rng.permutation(V)[:N].astype(np.int32)
+    head = dvl.Head(dev(w), V=V, d2t=dev(d2t))
+    assert dvl.draft_plan(head, M, 4) == ("bf16-tcgen05", 1)
+    L, _ = oracle_mod.logits_bf16(w, h)
+    ws = dvl.make_workspace(M, 4)
+    for _ in range(2):  # the group tickets leave the workspace clean
+        exact(dvl, oracle_mod, head, L, h, M, d2t, ws)

@@ -41,7 +41,8 @@ def test_exports_every_declared_symbol(dvl):
 def test_workspace_bytes(dvl):
     assert dvl.workspace_bytes(1, 1) == 512
     assert dvl.workspace_bytes(32, 1) == 512
-    assert dvl.workspace_bytes(3, 4) == 512 + 1024 * 3 * 4 * 8
+    # per-block lists for up to 1,024 blocks, 64 group lists, 64 group tickets
+    assert dvl.workspace_bytes(3, 4) == 512 + (1024 + 64) * 3 * 4 * 8 + 64 * 4
     assert dvl.workspace_bytes(0, 1) == 0
     assert dvl.workspace_bytes(33, 1) == 0
     assert dvl.workspace_bytes(1, 5) == 0
