@@ -3,7 +3,8 @@ block could stage when every hidden row sat in shared memory at once):
 bf16 at M = 32, K = 5,120 and at M = 20, K = 24,576 (one pass on the tcgen05
 kernel, which streams tiles of h with the head), and NVFP4 / FP8 at 9 to 32
 hidden rows (one pass at K = 2,560, groups of 16 rows at 5,120, on the
-low-bit kernel with two or four groups of 8 MMA columns).  Integer heads and
+low-bit kernel with two or four groups of 8 MMA columns), and 5 to 8 rows
+(one launch of its run-time-width instantiation).  Integer heads and
 hidden rows make every sum exact, so ids, logits and ties must agree with the
 oracle bit for bit; each case also checks the plan it ran on.  Gaussian
 NVFP4 / FP8 heads of the workloads' shapes (the 32,768 x 5,120 trimmed head,
@@ -82,8 +83,9 @@ def lowbit_int_head(dvl, oracle_mod, fmt, N, K, M, seed):
 
 
 @pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
-@pytest.mark.parametrize("K,M", [(2560, 9), (2560, 16), (2560, 17), (2560, 32),
-                                 (5120, 12), (5120, 16), (5120, 24), (5120, 32)])
+@pytest.mark.parametrize("K,M", [(2560, 5), (2560, 8), (2560, 9), (2560, 16), (2560, 17),
+                                 (2560, 32), (5120, 7), (5120, 12), (5120, 16), (5120, 24),
+                                 (5120, 32)])
 def test_lowbit_batched_one_pass(dvl, oracle_mod, fmt, K, M):
     # one launch for up to 32 rows (argmax) at 2,560, else one per 16 rows:
     # the head is read once per launch
