@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_mma_kernel(const ArgmaxArg
     static_assert(KC % kChunk == 0, "the width must be a multiple of the chunk");
     constexpr int CC = KC / kChunk;
     static_assert(CC % NB == 0, "the ring must divide the chunks");
+    static_assert(CC > NB, "the second part of h is waited for at chunk NB");
     constexpr int P = pitch<KC>();
     extern __shared__ __align__(16) unsigned char smem[];
     uint16_t *s_h = reinterpret_cast<uint16_t *>(smem);                          // [M][P]
@@ -151,20 +152,44 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_mma_kernel(const ArgmaxArg
     pdl_wait();
 
     // Copy the hidden rows into shared memory (16-byte asynchronous copies).
+    // At width 5,120 in two groups: the k-range of the first NB chunks,
+    // which the ring already holds, then the rest, which is waited for only
+    // before chunk NB of the first tile, so the MMAs on the buffered chunks
+    // overlap the second group's L2 round trip (0.65 us less per call on the
+    // 32,768-row trim at 3 and 4 rows; at 2,560 the mid-loop barrier cost
+    // more than it saved: +0.9 us at 16 rows on the 52,755-row head).
+    constexpr bool kSplit = KC >= 5120;
     {
-        constexpr int kVec = M * KC / 8;
-        for (int i = tid; i < kVec; i += kThreads) {
-            const int m = i / (KC / 8), e = 8 * (i - m * (KC / 8));
+        constexpr int kA = (kSplit ? NB * kChunk : KC) / 8;  // pieces per row, first group
+        for (int i = tid; i < M * kA; i += kThreads) {
+            const int m = i / kA, e = 8 * (i - m * kA);
+            cp_async16(s_h + m * P + e, a.h + (size_t)m * KC + e);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        constexpr int kB = KC / 8 - kA;      // the rest of each row
+        for (int i = tid; i < M * kB; i += kThreads) {
+            const int m = i / kB, e = 8 * (kA + i - m * kB);
             cp_async16(s_h + m * P + e, a.h + (size_t)m * KC + e);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
     for (int i = tid; i < M * kLists * KM; i += kThreads)
         s_cand[i] = 0ull;
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    if constexpr (kSplit)
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+        asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     if (!a.head_static)
         prologue();
+    // the block-wide wait for the second group: every thread reaches exactly
+    // one (here for a warp with no rows, else before chunk NB of tile 0)
+    auto rest_of_h = []() {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
+    };
+    if (kSplit && ntiles == 0)
+        rest_of_h();
 
     TopList<KM> best;
     best.init();
@@ -195,6 +220,8 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_mma_kernel(const ArgmaxArg
 #pragma unroll
         for (int c = 0; c < CC; ++c) {
             const int b = c % NB;
+            if (kSplit && c == NB && t == 0)
+                rest_of_h();
             // the hidden values of the same k as the lane's words
             uint4 hv[4], hv2[4];
 #pragma unroll
