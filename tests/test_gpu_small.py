@@ -41,6 +41,9 @@ CASES = [
     (64, 256, 1, "perm"), (257, 320, 3, "perm"), (1000, 64, 8, "none"),
     (3001, 256, 5, "perm"), (4099, 576, 1, "perm"), (777, 128, 9, "perm"),
     (2048, 192, 13, "none"), (513, 64, 32, "perm"), (20000, 128, 2, "perm"),
+    # short heads at the unrolled widths, one and two rows: the grid that
+    # gives every warp two full row groups (fewer blocks than the full grid)
+    (15000, 2560, 2, "perm"), (16000, 5120, 1, "none"),
 ]
 
 
