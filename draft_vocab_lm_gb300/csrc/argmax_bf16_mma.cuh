@@ -304,7 +304,7 @@ cudaError_t launch(const ArgmaxArgs &a, cudaStream_t s)
         return cudaErrorInvalidConfiguration;
     if (per_sm > 2)
         per_sm = 2;
-    long long grid = (long long)di.sms * per_sm;
+    long long grid = stream_grid(di.sms, per_sm);
     const long long max_by_rows = ((long long)a.N + kWarps - 1) / kWarps;  // >= 1 row per warp
     if (grid > max_by_rows)
         grid = max_by_rows;

@@ -682,7 +682,7 @@ cudaError_t launch_one(const ArgmaxArgs &a, cudaStream_t s)
         return cudaErrorInvalidConfiguration;
     if (per_sm > 512 / TH)
         per_sm = 512 / TH;
-    long long grid = (long long)di.sms * per_sm;
+    long long grid = stream_grid(di.sms, per_sm);
     // at least half an MMA tile of rows per warp on average
     const long long max_by_rows = ((long long)a.N + NW * 8 - 1) / (NW * 8);
     if (grid > max_by_rows)

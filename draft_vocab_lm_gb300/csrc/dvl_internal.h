@@ -50,6 +50,24 @@ struct DeviceInfo {
 };
 cudaError_t device_info(DeviceInfo *out);
 
+// Blocks of a streaming kernel that keeps per_sm blocks resident per SM:
+// all of them, except that with two or more per SM a few SMs (one in 38, at
+// least one) get one block fewer.  Measured on GB300 (152 SMs, so 300
+// blocks instead of 304), back-to-back calls: the full 248,320 x 2,560 head
+// at one row 178.6 -> 176.2 us, the 32,768 x 5,120 trim at one row 50.7 ->
+// 48.9 us and at three rows (register-path MMA) 53.4 -> 51.2 us, the FP8
+// full-vocabulary head 94.4 -> 93.3 us.  The gain is about the same number
+// of microseconds at every head size: with a few slots free from the start,
+// the next call's grid becomes resident (and starts its pre-wait loads)
+// while this one runs.
+inline long long stream_grid(int sms, int per_sm)
+{
+    long long g = (long long)sms * per_sm;
+    if (per_sm >= 2)
+        g -= sms / 38 > 1 ? sms / 38 : 1;
+    return g;
+}
+
 // Blocks of `func` (launched with `threads` threads and `smem` dynamic shared
 // bytes) resident per SM on the current device.  The first query per (kernel,
 // device, smem) also raises the kernel's dynamic shared-memory limit; the
