@@ -133,6 +133,16 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same MMA with a zero accumulator in.
+__device__ __forceinline__ void mma_f16_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 __device__ __forceinline__ float pow2f(int e)  // 2^e for e in [-126, 127], exact
 {
     return __int_as_float((127 + e) << 23);
@@ -476,6 +486,56 @@ __global__ void __launch_bounds__(block_threads<M, KC>(), 512 / block_threads<M,
             chunk_groups(qa, qb, sa, sb, cidx);
             return;
         }
+        if constexpr (kNv && M == 1) {
+            // One hidden row: the MMA's eight columns take the chunk's eight
+            // scale blocks instead.  MMA t pairs quad position q with k = 32 q
+            // + 4 t .. + 3 of both rows, which lie in block 2 q (t < 4) or
+            // 2 q + 1 (t >= 4); B puts h there in column 2 q or 2 q + 1 (the
+            // lanes g = 2 q, resp. 2 q + 1, hold it; every other B entry
+            // stays zero), so result column n is block n's dot of the
+            // unscaled codes.  Lane (g, q) holds columns 2 q, 2 q + 1 of rows
+            // g and g + 8: exactly the blocks its own two scale bytes per row
+            // cover, applied to the fp32 results (4 FMAs per chunk instead of
+            // 32 f16x2 multiplies).  The four lanes of a quad hold disjoint
+            // blocks of a row: summed at the end of the row group.
+            const uint4 *hp = s_h + (size_t)cidx * 16 + q;
+            if (g == 2 * q) {
+                const uint4 v0 = hp[0], v1 = hp[4];
+                hw[0] = v0.x; hw[1] = v0.y; hw[2] = v0.z; hw[3] = v0.w;
+                hw[4] = v1.x; hw[5] = v1.y; hw[6] = v1.z; hw[7] = v1.w;
+            } else if (g == 2 * q + 1) {
+                const uint4 v2 = hp[8], v3 = hp[12];
+                hw[8] = v2.x; hw[9] = v2.y; hw[10] = v2.z; hw[11] = v2.w;
+                hw[12] = v3.x; hw[13] = v3.y; hw[14] = v3.z; hw[15] = v3.w;
+            }
+            const uint32_t wa[4] = {qa[0].x, qa[0].y, qa[0].z, qa[0].w};
+            const uint32_t wb[4] = {qb[0].x, qb[0].y, qb[0].z, qb[0].w};
+            float p[2][4];  // two chains (MMAs t even / odd)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                uint32_t fa4[4], fb4[4];
+                e2m1_word(wa[u], fa4);
+                e2m1_word(wb[u], fb4);
+                if (u == 0) {
+                    mma_f16_zero(p[0], fa4[0], fb4[0], fa4[1], fb4[1], hw[0], hw[1]);
+                    mma_f16_zero(p[1], fa4[2], fb4[2], fa4[3], fb4[3], hw[2], hw[3]);
+                } else {
+                    mma_f16(p[0], fa4[0], fb4[0], fa4[1], fb4[1], hw[4 * u], hw[4 * u + 1]);
+                    mma_f16(p[1], fa4[2], fb4[2], fa4[3], fb4[3], hw[4 * u + 2], hw[4 * u + 3]);
+                }
+            }
+            uint32_t s2a, s2b;  // E4M3 pairs -> f16x2 (block 2 q low, 2 q + 1 high)
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2a) : "h"((uint16_t)sa));
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2b) : "h"((uint16_t)sb));
+            const __half2 ha = *reinterpret_cast<const __half2 *>(&s2a);
+            const __half2 hb = *reinterpret_cast<const __half2 *>(&s2b);
+            float(&c)[4] = acc[0][cidx & 3];
+            c[0] = fmaf(__low2float(ha), p[0][0] + p[1][0], c[0]);
+            c[0] = fmaf(__high2float(ha), p[0][1] + p[1][1], c[0]);
+            c[2] = fmaf(__low2float(hb), p[0][2] + p[1][2], c[2]);
+            c[2] = fmaf(__high2float(hb), p[0][3] + p[1][3], c[2]);
+            return;
+        }
         if (g < M) {
             const uint4 *hp = s_h + (size_t)cidx * (16 * M) + (g * 4 + q);
 #pragma unroll
@@ -545,6 +605,14 @@ __global__ void __launch_bounds__(block_threads<M, KC>(), 512 / block_threads<M,
 #pragma unroll
                 for (int c = 0; c < CH; ++c)
                     acc[G][c][j] = 0.f;
+            }
+            if constexpr (kNv && M == 1 && NG == 1) {
+                // one hidden row: the quad's four lanes hold disjoint blocks
+#pragma unroll
+                for (int j = 0; j < 4; j += 2) {
+                    d[j] += __shfl_xor_sync(kFull, d[j], 1);
+                    d[j] += __shfl_xor_sync(kFull, d[j], 2);
+                }
             }
             const int m0 = 8 * G + 2 * q;
             if (ra < rend) {

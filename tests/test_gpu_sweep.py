@@ -66,6 +66,11 @@ def _cases():
         k = int(min(rng.integers(1, 5), N))
         mode = ["none", "d2t", "base"][int(rng.integers(0, 3))]
         out.append((i, dtype, N, K, M, k, mode))
+    # NVFP4 at one hidden row and the unrolled widths (block scales applied
+    # to the MMA results): heads long enough for every warp of the full grid
+    # to take one or two 16-row tiles
+    out += [(40, "nvfp4", 40000, 2560, 1, 4, "d2t"), (41, "nvfp4", 20000, 5120, 1, 1, "base"),
+            (42, "nvfp4", 20000, 5120, 1, 3, "none")]
     return out
 
 
