@@ -129,9 +129,42 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
     // From here on: inputs and workspace that earlier work may have written.
     pdl_wait();
 
+    // Three hidden rows at width 2,560: h is staged in two parts.  The k
+    // range of the first NB steps is stored before the main loop; the rest
+    // is loaded up front into registers and stored at one block barrier
+    // before step NB of the first group, so its stores wait behind the
+    // first steps' arithmetic (16,000-row shortlist: 15.7 -> 15.3 us per
+    // call; four rows would spill).
+    constexpr bool kSplitH = KC == 2560 && M == 3;
+    constexpr int kUA = kSplitH ? NB * 32 : 0;  // 16-byte units per row in the first part
+    constexpr int kPerB = KC / 8 - kUA;         // and in the rest (used when kSplitH)
+    constexpr int kPB = kSplitH ? (M * kPerB + kThreads - 1) / kThreads : 1;
+    uint4 vb[kPB];
+    auto store_unit = [&](int m, int e, const uint4 &x) {
+        float *dst = s_h + m * Kpad + (e & ~255) + ((e & 255) >> 3) * 4;
+        *reinterpret_cast<float4 *>(dst) =
+            make_float4(bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y));
+        *reinterpret_cast<float4 *>(dst + 128) =
+            make_float4(bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w));
+    };
+    if constexpr (kSplitH) {
+#pragma unroll
+        for (int u = 0; u < kPB; ++u) {
+            const int i = tid + u * kThreads;
+            vb[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < M * kPerB) {
+                const int m = i / kPerB, e = 8 * (kUA + i - m * kPerB);
+                vb[u] = __ldg(reinterpret_cast<const uint4 *>(a.h + (size_t)m * K + e));
+            }
+        }
+        for (int i = tid; i < M * kUA; i += kThreads) {
+            const int m = i / kUA, e = 8 * (i - m * kUA);
+            store_unit(m, e, __ldg(reinterpret_cast<const uint4 *>(a.h + (size_t)m * K + e)));
+        }
+    }
     // Stage the hidden rows (bf16 -> fp32, zero past K): 16-byte loads, all
     // of a thread's loads issued before its shared-memory stores.
-    {
+    if constexpr (!kSplitH) {
         constexpr int kMaxPer = 10;  // covers M * Kpad <= 10 * 8 * 256 (four rows of 5,120)
         const int nvec = M * (Kpad / 8);
         uint4 v[kMaxPer];
@@ -152,11 +185,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
             if (i < nvec) {
                 const int m = i / (Kpad / 8);
                 const int e = 8 * (i - m * (Kpad / 8));
-                float *dst = s_h + m * Kpad + (e & ~255) + ((e & 255) >> 3) * 4;
-                *reinterpret_cast<float4 *>(dst) =
-                    make_float4(bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y));
-                *reinterpret_cast<float4 *>(dst + 128) =
-                    make_float4(bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w));
+                store_unit(m, e, v[u]);
             }
         }
         for (int i = tid + kMaxPer * kThreads; i < nvec; i += kThreads) {
@@ -165,11 +194,7 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
             uint4 x = make_uint4(0u, 0u, 0u, 0u);
             if (e < K)
                 x = __ldg(reinterpret_cast<const uint4 *>(a.h + (size_t)m * K + e));
-            float *dst = s_h + m * Kpad + (e & ~255) + ((e & 255) >> 3) * 4;
-            *reinterpret_cast<float4 *>(dst) =
-                make_float4(bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y));
-            *reinterpret_cast<float4 *>(dst + 128) =
-                make_float4(bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w));
+            store_unit(m, e, x);
         }
     }
     for (int i = tid; i < M * kLists * KM; i += kThreads)
@@ -177,6 +202,23 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
     __syncthreads();
     if (!a.head_static)
         prologue();
+    // the second part of h; every thread reaches exactly one call (a warp
+    // without rows here, the others before step NB of their first group)
+    auto rest_of_h = [&]() {
+        if constexpr (kSplitH) {
+#pragma unroll
+            for (int u = 0; u < kPB; ++u) {
+                const int i = tid + u * kThreads;
+                if (i < M * kPerB) {
+                    const int m = i / kPerB, e = 8 * (kUA + i - m * kPerB);
+                    store_unit(m, e, vb[u]);
+                }
+            }
+            __syncthreads();
+        }
+    };
+    if (kSplitH && ngroups == 0)
+        rest_of_h();
 
     // Which (row slot, hidden row) this lane owns after the reduce-scatter.
     constexpr int NV = RPW * M;
@@ -235,6 +277,8 @@ __global__ void __launch_bounds__(kThreads, 2) argmax_bf16_kernel(const ArgmaxAr
 #pragma unroll
             for (int j = 0; j < JC; ++j) {
                 const int b = j % NB;
+                if (kSplitH && j == NB && g == 0)
+                    rest_of_h();
                 fma_step<RPW, M>(acc, buf[b], hp + j * kKStep, KC);
                 const int jj = j + NB;
 #pragma unroll

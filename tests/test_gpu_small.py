@@ -44,6 +44,9 @@ CASES = [
     # short heads at the unrolled widths, one and two rows: the grid that
     # gives every warp two full row groups (fewer blocks than the full grid)
     (15000, 2560, 2, "perm"), (16000, 5120, 1, "none"),
+    # three rows at 2,560: h staged in two parts around a block barrier,
+    # reached by warps without rows too (40 rows leave most of them empty)
+    (16000, 2560, 3, "perm"), (40, 2560, 3, "none"),
 ]
 
 
