@@ -45,8 +45,11 @@ def score_bytes(M: int, c: int, K: int, dtype: str = "bf16") -> int:
 
 def quantize_bytes(N: int, K: int, dtype: str) -> int:
     """Algorithmic bytes of requantizing a bf16 N x K head: the head read
-    twice (its maximum, then the codes) and the NVFP4 or FP8 head written."""
-    return 2 * N * K * 2 + head_bytes(N, K, dtype) - 4
+    once and the NVFP4 or FP8 head written.  (The recipe needs the head's
+    maximum before any code, so a head larger than L2 is read twice: its
+    traffic is N K 2 bytes more, and half the copy peak is its ceiling on
+    this count.)"""
+    return N * K * 2 + head_bytes(N, K, dtype) - 4
 
 
 def call_flops(N: int, K: int, M: int) -> int:
