@@ -28,8 +28,11 @@
 //   - NVFP4: each code byte becomes an f16 pair with the exact E2M1x2 ->
 //     f16x2 conversion and is multiplied by its block's E4M3 scale (E4M3x2 ->
 //     f16x2); the product has at most 6 significant bits and lies in
-//     [2^-10, 2688], so it is exact in f16.  FP8: each pair of code bytes
-//     becomes an f16 pair with the exact E4M3x2 -> f16x2 conversion;
+//     [2^-10, 2688], so it is exact in f16.  With one hidden row the MMA's
+//     eight columns carry the chunk's eight scale blocks instead, and the
+//     scales multiply the fp32 block dots (see chunk()).  FP8: each pair
+//     of code bytes becomes an f16 pair with the exact E4M3x2 -> f16x2
+//     conversion;
 //   - the hidden rows are staged once per block as f16 after an exact
 //     power-of-two rescale that puts their largest magnitude in [2^14, 2^15)
 //     (bf16 values within 2^31 of that maximum convert exactly; smaller ones
