@@ -300,3 +300,19 @@ def test_call_stream_handle_without_a_device(dvl, monkeypatch):
     monkeypatch.setattr(d, "_raw_stream_fn", lambda dev_index: 4242 + dev_index)
     t.get_device = lambda: 0  # a CPU tensor reports -1
     assert d._call_stream(None, t) == 4242
+
+
+def test_noalloc_checks_reject_before_any_launch(dvl):
+    # the fixed scratch holds at most DVL_MAX_M rows; bad heads and pointers
+    # fail before the scratch is looked up (no device needed)
+    from draft_vocab_lm_gb300._native import lib
+    L = lib()
+    good, bad = _head(), _head(K=100)
+    for M in (0, -1, 33):
+        assert L.dvl_draft_argmax_noalloc(ctypes.byref(good), 0x3000, M, 0x2000, 0x4000, None) == 1
+    assert L.dvl_draft_argmax_noalloc(ctypes.byref(bad), 0x3000, 1, 0x2000, 0x4000, None) == 1
+    assert L.dvl_draft_argmax_noalloc(ctypes.byref(good), None, 1, 0x2000, 0x4000, None) == 1
+    assert L.dvl_draft_argmax_noalloc(ctypes.byref(good), 0x3008, 1, 0x2000, 0x4000, None) == 1
+    assert L.dvl_draft_argmax_noalloc(ctypes.byref(good), 0x3000, 1, None, 0x4000, None) == 1
+    assert L.dvl_draft_argmax_noalloc(ctypes.byref(good), 0x3000, 1, 0x2000, 0x4002, None) == 1
+    assert L.dvl_noalloc_status(None, None) == 1
