@@ -163,30 +163,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ---- TMA producer ----
+        // Stage i (tile i / nst, k boxes from (i % nst) * kBoxes): the W
+        // boxes and the h boxes of a stage complete one barrier phase
+        // together (one arrival, their bytes expected up front).  A head
+        // the caller marked static fills the first S stages' W boxes before
+        // the wait for the preceding kernel, their h boxes after it.
         if (lane == 0) {
+            const int nst = (KC + L::kBoxes - 1) / L::kBoxes, total = ntiles * nst;
+            auto boxes = [&](int i) { return min(L::kBoxes, KC - (i % nst) * L::kBoxes); };
+            auto expect = [&](int i, int s) {
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(boxes(i) * (kWTile + L::kHTile)));
+            };
+            auto load_w = [&](int i, int s) {
+                const int row = r0 + (i / nst) * kBM, kc = (i % nst) * L::kBoxes;
+                for (int bx = 0; bx < boxes(i); ++bx)
+                    tc::tma_load_2d(sW + (size_t)s * L::kWStage + bx * kWTile, &tmap_w,
+                                    (kc + bx) * kBK, row, &full[s]);
+            };
+            auto load_h = [&](int i, int s) {
+                const int kc = (i % nst) * L::kBoxes;
+                for (int bx = 0; bx < boxes(i); ++bx)
+                    tc::tma_load_2d(sH + (size_t)s * L::kHStage + bx * L::kHTile, &tmap_h,
+                                    (kc + bx) * kBK, 0, &full[s]);
+            };
+            const int pre = a.head_static ? min(S, total) : 0;
+            for (int i = 0; i < pre; ++i) {  // fresh barriers: no wait for the stage
+                expect(i, i);
+                load_w(i, i);
+            }
             pdl_wait();
-            uint32_t i = 0;
-            for (int t = 0; t < ntiles; ++t) {
-                const int row = r0 + t * kBM;
-                bool ok = true;
-                for (int kc = 0; kc < KC; kc += L::kBoxes, ++i) {
-                    const int s = (int)(i % S);
-                    if (!wait_or_abort(&empty[s], ((i / S) & 1u) ^ 1u, abort_flag, a.ws)) {
-                        ok = false;
-                        break;
-                    }
-                    const int nb = min(L::kBoxes, KC - kc);
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(nb * (kWTile + L::kHTile)));
-                    for (int bx = 0; bx < nb; ++bx) {
-                        tc::tma_load_2d(sW + (size_t)s * L::kWStage + bx * kWTile, &tmap_w,
-                                        (kc + bx) * kBK, row, &full[s]);
-                        tc::tma_load_2d(sH + (size_t)s * L::kHStage + bx * L::kHTile, &tmap_h,
-                                        (kc + bx) * kBK, 0, &full[s]);
-                    }
-                    misc[2] = i + 1;
-                }
-                if (!ok)
+            for (int i = 0; i < pre; ++i) {
+                load_h(i, i);
+                misc[2] = i + 1;
+            }
+            for (int i = pre; i < total; ++i) {
+                const int s = i % S;
+                if (!wait_or_abort(&empty[s], ((i / S) & 1u) ^ 1u, abort_flag, a.ws))
                     break;
+                expect(i, s);
+                load_w(i, s);
+                load_h(i, s);
+                misc[2] = i + 1;
             }
         }
     } else if (warp == 1) {
