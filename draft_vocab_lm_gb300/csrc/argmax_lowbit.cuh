@@ -302,12 +302,13 @@ __global__ void __launch_bounds__(block_threads<M, KC>(), 512 / block_threads<M,
         // rounds of four per thread (16-byte loads, then stores; the load
         // ring holds most registers; rows past MR stay zero), read in h's
         // own order so that a warp reads 512 contiguous bytes, each placed
-        // at its unit's slot; the maximum is read back from there, and each
-        // thread converts its units in place.  (cp.async copies instead:
-        // 36.9 against 32.8 us for NVFP4 32,768 x 5,120 at 16 rows, 145.1
-        // against 137.1 for FP8 248,320 x 2,560 at 32.)
+        // at its unit's slot; the maximum is taken from the registers on the
+        // way, and each thread then converts its units in place.  (cp.async
+        // copies instead: 36.9 against 32.8 us for NVFP4 32,768 x 5,120 at
+        // 16 rows, 145.1 against 137.1 for FP8 248,320 x 2,560 at 32.)
         constexpr int kUnits = (KC / kChunk) * 16 * M;
         constexpr int kRound = 4;
+        unsigned int mx = 0u;  // the maximum, from the registers as they are stored
         for (int i0 = 0; i0 < kUnits; i0 += kRound * TH) {
             uint4 v[kRound];
             int sl[kRound];
@@ -325,20 +326,16 @@ __global__ void __launch_bounds__(block_threads<M, KC>(), 512 / block_threads<M,
             }
 #pragma unroll
             for (int u = 0; u < kRound; ++u)
-                if (sl[u] >= 0)
+                if (sl[u] >= 0) {
                     s_h[sl[u]] = v[u];
-        }
-        __syncthreads();  // units land in other threads' slots
-        unsigned int mx = 0u;
-        for (int i = tid; i < kUnits; i += TH) {
-            const uint4 x = s_h[i];
-            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                    const uint32_t xs[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-                mx = max(mx, max(xs[t] & 0x7fffu, (xs[t] >> 16) & 0x7fffu));
+                    for (int t = 0; t < 4; ++t)
+                        mx = max(mx, max(xs[t] & 0x7fffu, (xs[t] >> 16) & 0x7fffu));
+                }
         }
         block_max(mx);
-        __syncthreads();
+        __syncthreads();  // units land in other threads' slots; the warp maxima
         shift = shift_of(read_max());
         const float up = shift >= 0 ? pow2f(min(shift, 127)) : pow2f(max(shift, -126));
         for (int i = tid; i < kUnits; i += TH)
